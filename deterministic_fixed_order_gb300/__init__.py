@@ -1,0 +1,251 @@
+"""Python binding of libdetfold, the fixed-order elementwise fold for GB300.
+
+Argument marshalling only: every step of the fold runs in the CUDA library
+(``libdetfold.so``, built in-tree from ``csrc/`` by ``build.build()``). If
+the library has not been built this module raises on import; there is no
+CPU fallback.
+
+The functions keep the C names of ``include/detfold.h``. Device operands may
+be given as CUDA float32 tensors (checked for device, dtype, contiguity and
+size against the lengths passed) or as raw integer addresses (passed through
+unchecked). ``stream`` may be None (torch's current stream), a
+``torch.cuda.Stream`` or a raw handle. A negative status raises
+``DetfoldError``; the ``status_*`` variants return it instead.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "DetfoldError", "lib", "DETFOLD_MAX_W", "DETFOLD_MAX_LEN",
+    "DETFOLD_STAGED_REVERSE_DELIVERY", "DETFOLD_STAGED_SEPARATE_SCALE",
+    "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
+    "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
+    "detfold_loopback_allreduce_staged", "detfold_shard_plan",
+    "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
+    "STATUS",
+]
+
+LIB_PATH = _build.LIB
+
+DETFOLD_MAX_W = 256
+DETFOLD_MAX_LEN = 1 << 40
+DETFOLD_STAGED_REVERSE_DELIVERY = 1
+DETFOLD_STAGED_SEPARATE_SCALE = 2
+
+STATUS = {
+    "DETFOLD_OK": 0, "DETFOLD_ERR_NULL": -1, "DETFOLD_ERR_WORLD": -2, "DETFOLD_ERR_LEN": -3,
+    "DETFOLD_ERR_ALIGN": -4, "DETFOLD_ERR_OVERLAP": -5, "DETFOLD_ERR_WORKSPACE": -6,
+    "DETFOLD_ERR_CUDA": -7, "DETFOLD_ERR_ARG": -8,
+}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libdetfold.so is not built ({LIB_PATH}); run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` first")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_F = ctypes.c_float
+
+lib.detfold_sum_stacked.argtypes = [_P, _P, _INT, _I64, _P]
+lib.detfold_sum_ptrs.argtypes = [_P, _P, _INT, _I64, _P]
+lib.detfold_scale.argtypes = [_P, _I64, _F, _P]
+lib.detfold_loopback_allreduce.argtypes = [_P, _INT, _I64, _F, _P]
+lib.detfold_staged_workspace_bytes.argtypes = [_I64, _INT]
+lib.detfold_staged_workspace_bytes.restype = _I64
+lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _INT, _P, _I64, _P]
+lib.detfold_shard_plan.argtypes = [_I64, _INT, _P, _P]
+lib.detfold_status_string.argtypes = [_INT]
+lib.detfold_status_string.restype = ctypes.c_char_p
+lib.detfold_last_cuda_error.argtypes = []
+lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
+for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
+              "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
+              "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
+    getattr(lib, _name).restype = _INT
+
+
+class DetfoldError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib.detfold_status_string(status).decode()
+        if status == STATUS["DETFOLD_ERR_CUDA"]:
+            msg += f" (cudaError {lib.detfold_last_cuda_error()})"
+        super().__init__(f"{where}: status {status}: {msg}")
+        self.status = status
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise DetfoldError(status, where)
+
+
+def _dev_ptr(x, need_elems: int | None, what: str) -> int:
+    """Address of a device operand; tensors are checked against need_elems."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{what}: expected a CUDA float32 tensor or an int address")
+    if not x.is_cuda or x.dtype != torch.float32:
+        raise TypeError(f"{what}: expected a CUDA float32 tensor, got {x.device} {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{what}: tensor must be contiguous")
+    if need_elems is not None and x.numel() < need_elems:
+        raise ValueError(f"{what}: tensor holds {x.numel()} elements, call needs {need_elems}")
+    return x.data_ptr()
+
+
+def _stream(s) -> int:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _ptr_array(items, need_elems, what):
+    ptrs = [_dev_ptr(t, need_elems, f"{what}[{k}]") for k, t in enumerate(items)]
+    return (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
+
+
+# ------------------------------------------------------------------ status-returning calls
+
+def status_sum_stacked(out, stacked, W: int, length: int, stream=None) -> int:
+    return lib.detfold_sum_stacked(_dev_ptr(out, length, "out"),
+                                   _dev_ptr(stacked, W * length, "stacked"),
+                                   W, length, _stream(stream))
+
+
+def status_sum_ptrs(out, srcs, W: int, length: int, stream=None) -> int:
+    tab = _ptr_array(srcs, length, "srcs") if srcs is not None else None
+    return lib.detfold_sum_ptrs(_dev_ptr(out, length, "out"), tab, W, length, _stream(stream))
+
+
+def status_scale(buf, length: int, scale: float, stream=None) -> int:
+    return lib.detfold_scale(_dev_ptr(buf, length, "buf"), length, scale, _stream(stream))
+
+
+def status_loopback_allreduce(arenas, W: int, length: int, mean_scale: float = 1.0,
+                              stream=None) -> int:
+    tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
+    return lib.detfold_loopback_allreduce(tab, W, length, mean_scale, _stream(stream))
+
+
+def status_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: float, flags: int,
+                                     workspace, workspace_bytes: int, stream=None) -> int:
+    tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
+    ws = workspace
+    if ws is not None and not isinstance(ws, int):
+        import torch
+        if not ws.is_cuda or not ws.is_contiguous():
+            raise ValueError("workspace: expected a contiguous CUDA tensor")
+        if ws.numel() * ws.element_size() < workspace_bytes:
+            raise ValueError("workspace: tensor smaller than workspace_bytes")
+        ws = ws.data_ptr()
+    return lib.detfold_loopback_allreduce_staged(tab, W, length, mean_scale, flags, ws or 0,
+                                                 workspace_bytes, _stream(stream))
+
+
+# ------------------------------------------------------------------ raising calls (C names)
+
+def detfold_sum_stacked(out, stacked, W: int, length: int, stream=None) -> None:
+    _check(status_sum_stacked(out, stacked, W, length, stream), "detfold_sum_stacked")
+
+
+def detfold_sum_ptrs(out, srcs, W: int, length: int, stream=None) -> None:
+    _check(status_sum_ptrs(out, srcs, W, length, stream), "detfold_sum_ptrs")
+
+
+def detfold_scale(buf, length: int, scale: float, stream=None) -> None:
+    _check(status_scale(buf, length, scale, stream), "detfold_scale")
+
+
+def detfold_loopback_allreduce(arenas, W: int, length: int, mean_scale: float = 1.0,
+                               stream=None) -> None:
+    _check(status_loopback_allreduce(arenas, W, length, mean_scale, stream),
+           "detfold_loopback_allreduce")
+
+
+def detfold_staged_workspace_bytes(length: int, W: int) -> int:
+    n = lib.detfold_staged_workspace_bytes(length, W)
+    _check(n if n < 0 else 0, "detfold_staged_workspace_bytes")
+    return n
+
+
+def detfold_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: float = 1.0,
+                                      flags: int = 0, workspace=None, workspace_bytes: int = 0,
+                                      stream=None) -> None:
+    _check(status_loopback_allreduce_staged(arenas, W, length, mean_scale, flags, workspace,
+                                            workspace_bytes, stream),
+           "detfold_loopback_allreduce_staged")
+
+
+def detfold_shard_plan(length: int, W: int) -> tuple[list[int], list[int]]:
+    starts = (ctypes.c_int64 * max(1, W))()
+    lens = (ctypes.c_int64 * max(1, W))()
+    _check(lib.detfold_shard_plan(length, W, starts, lens), "detfold_shard_plan")
+    return list(starts)[:W], list(lens)[:W]
+
+
+def detfold_status_string(status: int) -> str:
+    return lib.detfold_status_string(status).decode()
+
+
+def detfold_last_cuda_error() -> int:
+    return lib.detfold_last_cuda_error()
+
+
+def detfold_launch_floor(count: int, pdl: int = 1, stream=None) -> None:
+    _check(lib.detfold_launch_floor(count, pdl, _stream(stream)), "detfold_launch_floor")
+
+
+# ------------------------------------------------------------------ tensor conveniences
+
+def sum_stacked(stacked, out=None, stream=None):
+    """out = fold of the rows of a [W, len] CUDA float32 tensor."""
+    import torch
+    W, n = stacked.shape
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=stacked.device)
+    detfold_sum_stacked(out, stacked, W, n, stream)
+    return out
+
+
+def sum_ptrs(srcs, out=None, stream=None):
+    import torch
+    n = srcs[0].numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=srcs[0].device)
+    detfold_sum_ptrs(out, list(srcs), len(srcs), n, stream)
+    return out
+
+
+def loopback_allreduce(arenas, mean: bool = False, stream=None) -> None:
+    W = len(arenas)
+    scale = float(_mean_scale(W)) if mean else 1.0
+    detfold_loopback_allreduce(list(arenas), W, arenas[0].numel(), scale, stream)
+
+
+def _mean_scale(W: int):
+    # fl(1/W) in binary32: a host-side argument value, computed by the caller.
+    import numpy as np
+    return np.float32(1.0) / np.float32(W)
+
+
+def mean_scale(W: int) -> float:
+    """fl(1/W) in binary32, the scale the mean multiplies by."""
+    return float(_mean_scale(W))
+
+
+def shard_plan(length: int, W: int):
+    return detfold_shard_plan(length, W)

@@ -1,0 +1,285 @@
+// The C ABI of libdetfold (declared in include/detfold.h): argument
+// validation, the shard plan, dispatch to the fold launchers, and the staged
+// comparator's copy schedule. Nothing here allocates, synchronizes or
+// touches device memory other than through stream-ordered launches and
+// copies.
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "detfold.h"
+#include "detfold_launch.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return DETFOLD_OK;
+    g_last_cuda_error = (int)e;
+    (void)cudaGetLastError();  // clear a non-sticky launch error
+    return DETFOLD_ERR_CUDA;
+}
+
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+// Half-open byte ranges [a, a+na) and [b, b+nb) intersect.
+bool intersects(const void *a, int64_t na, const void *b, int64_t nb)
+{
+    const uintptr_t ua = (uintptr_t)a, ub = (uintptr_t)b;
+    return ua < ub + (uintptr_t)nb && ub < ua + (uintptr_t)na;
+}
+
+int check_world(int W) { return (W < 1 || W > DETFOLD_MAX_W) ? DETFOLD_ERR_WORLD : DETFOLD_OK; }
+
+int check_len(int64_t len) { return (len < 0 || len > DETFOLD_MAX_LEN) ? DETFOLD_ERR_LEN : DETFOLD_OK; }
+
+void plan_shards(int64_t len, int W, int64_t *starts, int64_t *lens)
+{
+    const int64_t base = len / W, rem = len % W;
+    for (int r = 0; r < W; ++r) {
+        starts[r] = (int64_t)r * base + (r < rem ? r : rem);
+        lens[r] = base + (r < rem ? 1 : 0);
+    }
+}
+
+// Stack row stride (elements) of the staged comparator: the largest shard
+// plus room to shift a row by up to 7 elements, rounded to 64 elements.
+int64_t staged_row_stride(int64_t len, int W)
+{
+    const int64_t max_shard = (len + W - 1) / W;
+    return (max_shard + 8 + 63) / 64 * 64;
+}
+
+cudaError_t launch(const detfold::LaunchSpec &s, cudaStream_t st)
+{
+    switch (s.mode) {
+    case detfold::kSumNC: return detfold::launch_sum_nc(s, st);
+    case detfold::kSumCoherent: return detfold::launch_sum_coherent(s, st);
+    default: return detfold::launch_allreduce(s, st);
+    }
+}
+
+int arenas_valid(float *const *arenas, int W, int64_t len)
+{
+    if (!arenas) return DETFOLD_ERR_NULL;
+    for (int r = 0; r < W; ++r)
+        if (!arenas[r]) return DETFOLD_ERR_NULL;
+    for (int r = 0; r < W; ++r)
+        if (!aligned4(arenas[r])) return DETFOLD_ERR_ALIGN;
+    const int64_t bytes = len * 4;
+    for (int a = 0; a < W; ++a)
+        for (int b = a + 1; b < W; ++b)
+            if (arenas[a] == arenas[b] || intersects(arenas[a], bytes, arenas[b], bytes))
+                return DETFOLD_ERR_OVERLAP;
+    return DETFOLD_OK;
+}
+
+__global__ void empty_kernel(int pdl)
+{
+    if (pdl) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+}
+
+}  // namespace
+
+namespace detfold {
+
+cudaError_t launch_empty(int count, int pdl, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    for (int k = 0; k < count; ++k) {
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, empty_kernel, pdl);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace detfold
+
+extern "C" {
+
+int detfold_sum_stacked(float *out, const float *stacked, int W, int64_t len, void *stream)
+{
+    if (!out || !stacked) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    if (!aligned4(out) || !aligned4(stacked)) return DETFOLD_ERR_ALIGN;
+    if (len == 0) return DETFOLD_OK;
+    if (intersects(out, len * 4, stacked, (int64_t)W * len * 4)) return DETFOLD_ERR_OVERLAP;
+    const float *rows[DETFOLD_MAX_W];
+    for (int r = 0; r < W; ++r) rows[r] = stacked + (int64_t)r * len;
+    detfold::LaunchSpec s = {W, detfold::kSumNC, rows, out, len, 1.0f, 0};
+    return cuda_status(launch(s, (cudaStream_t)stream));
+}
+
+int detfold_sum_ptrs(float *out, const float *const *srcs, int W, int64_t len, void *stream)
+{
+    if (!out || !srcs) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    for (int r = 0; r < W; ++r)
+        if (!srcs[r]) return DETFOLD_ERR_NULL;
+    if (int rc = check_len(len)) return rc;
+    if (!aligned4(out)) return DETFOLD_ERR_ALIGN;
+    for (int r = 0; r < W; ++r)
+        if (!aligned4(srcs[r])) return DETFOLD_ERR_ALIGN;
+    if (len == 0) return DETFOLD_OK;
+    bool in_place = false;
+    for (int r = 0; r < W; ++r) {
+        if (srcs[r] == out) {
+            in_place = true;
+        } else if (intersects(out, len * 4, srcs[r], len * 4)) {
+            return DETFOLD_ERR_OVERLAP;
+        }
+    }
+    if (W == 1 && in_place) return DETFOLD_OK;  // the fold of one addend is itself
+    detfold::LaunchSpec s = {W, in_place ? detfold::kSumCoherent : detfold::kSumNC, srcs, out, len,
+                             1.0f, 0};
+    return cuda_status(launch(s, (cudaStream_t)stream));
+}
+
+int detfold_scale(float *buf, int64_t len, float scale, void *stream)
+{
+    if (!buf) return DETFOLD_ERR_NULL;
+    if (int rc = check_len(len)) return rc;
+    if (!aligned4(buf)) return DETFOLD_ERR_ALIGN;
+    if (len == 0 || scale == 1.0f) return DETFOLD_OK;
+    const float *one[1] = {buf};
+    detfold::LaunchSpec s = {1, detfold::kAllReduce, one, nullptr, len, scale, 1};
+    return cuda_status(launch(s, (cudaStream_t)stream));
+}
+
+int detfold_loopback_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
+                               void *stream)
+{
+    if (!arenas) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    if (int rc = arenas_valid(arenas, W, len)) return rc;
+    if (len == 0) return DETFOLD_OK;
+    const int do_scale = mean_scale != 1.0f;
+    if (W == 1 && !do_scale) return DETFOLD_OK;
+    detfold::LaunchSpec s = {W, detfold::kAllReduce, (const float *const *)arenas, nullptr, len,
+                             mean_scale, do_scale};
+    return cuda_status(launch(s, (cudaStream_t)stream));
+}
+
+int64_t detfold_staged_workspace_bytes(int64_t len, int W)
+{
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    return ((int64_t)W * staged_row_stride(len, W) + 8) * 4;
+}
+
+int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len, float mean_scale,
+                                      int flags, void *workspace, int64_t workspace_bytes,
+                                      void *stream)
+{
+    if (!arenas) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    if (flags & ~(DETFOLD_STAGED_REVERSE_DELIVERY | DETFOLD_STAGED_SEPARATE_SCALE))
+        return DETFOLD_ERR_ARG;
+    if (int rc = arenas_valid(arenas, W, len)) return rc;
+    const bool do_scale = mean_scale != 1.0f;
+    if (len == 0) return DETFOLD_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (W == 1) {
+        // The reference's round is a no-op for one rank; only the mean remains.
+        return detfold_scale(arenas[0], len, mean_scale, stream);
+    }
+    const int64_t need = detfold_staged_workspace_bytes(len, W);
+    if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 15u))
+        return DETFOLD_ERR_WORKSPACE;
+    for (int r = 0; r < W; ++r)
+        if (intersects(workspace, workspace_bytes, arenas[r], len * 4)) return DETFOLD_ERR_OVERLAP;
+
+    int64_t starts[DETFOLD_MAX_W], lens[DETFOLD_MAX_W];
+    plan_shards(len, W, starts, lens);
+    const int64_t stride = staged_row_stride(len, W);
+    float *ws = (float *)(((uintptr_t)workspace + 31u) & ~(uintptr_t)31u);
+    const bool reverse = flags & DETFOLD_STAGED_REVERSE_DELIVERY;
+    const bool separate = flags & DETFOLD_STAGED_SEPARATE_SCALE;
+
+    // Phase A: per owner, exchange into slot = source rank, then fold.
+    for (int o = 0; o < W; ++o) {
+        const int64_t n = lens[o], s0 = starts[o];
+        if (n == 0) continue;
+        float *dst = arenas[o] + s0;
+        const int ph = detfold::elem_phase(dst, 8);  // rows share the shard's 32-byte phase
+        const float *rows[DETFOLD_MAX_W];
+        for (int r = 0; r < W; ++r) rows[r] = ws + (int64_t)r * stride + ph;
+        for (int k = 0; k < W; ++k) {
+            const int src = reverse ? W - 1 - k : k;
+            cudaError_t e = cudaMemcpyAsync((void *)rows[src], arenas[src] + s0, (size_t)n * 4,
+                                            cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        detfold::LaunchSpec s = {W, detfold::kSumNC, rows, dst, n, mean_scale,
+                                 (do_scale && !separate) ? 1 : 0};
+        if (int rc = cuda_status(launch(s, st))) return rc;
+        if (do_scale && separate) {
+            if (int rc = detfold_scale(dst, n, mean_scale, stream)) return rc;
+        }
+    }
+    // Phase B: every owner's shard to every other arena.
+    for (int o = 0; o < W; ++o) {
+        const int64_t n = lens[o], s0 = starts[o];
+        if (n == 0) continue;
+        for (int r = 0; r < W; ++r) {
+            if (r == o) continue;
+            cudaError_t e = cudaMemcpyAsync(arenas[r] + s0, arenas[o] + s0, (size_t)n * 4,
+                                            cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+    }
+    return DETFOLD_OK;
+}
+
+int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens)
+{
+    if (!starts || !lens) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    plan_shards(len, W, starts, lens);
+    return DETFOLD_OK;
+}
+
+const char *detfold_status_string(int status)
+{
+    switch (status) {
+    case DETFOLD_OK: return "ok";
+    case DETFOLD_ERR_NULL: return "a required pointer is NULL";
+    case DETFOLD_ERR_WORLD: return "W is outside [1, DETFOLD_MAX_W]";
+    case DETFOLD_ERR_LEN: return "len is negative or above DETFOLD_MAX_LEN";
+    case DETFOLD_ERR_ALIGN: return "a device pointer is not 4-byte aligned";
+    case DETFOLD_ERR_OVERLAP: return "operands overlap in a way this call forbids";
+    case DETFOLD_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
+    case DETFOLD_ERR_CUDA: return "a CUDA call failed (see detfold_last_cuda_error)";
+    case DETFOLD_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+    }
+}
+
+int detfold_last_cuda_error(void) { return g_last_cuda_error; }
+
+int detfold_launch_floor(int count, int pdl, void *stream)
+{
+    if (count < 0) return DETFOLD_ERR_ARG;
+    return cuda_status(detfold::launch_empty(count, pdl ? 1 : 0, (cudaStream_t)stream));
+}
+
+}  // extern "C"

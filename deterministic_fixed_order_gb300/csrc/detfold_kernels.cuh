@@ -1,0 +1,312 @@
+// Device side of libdetfold: the fixed-order fold kernels for sm_103a.
+//
+// One kernel family covers every fold of the library. Each thread owns whole
+// output elements; for each it loads the W addends (all loads of an unrolled
+// group are issued before any add), then runs the serial chain
+//     acc = s_0; acc = __fadd_rn(acc, s_r) for r = 1..W-1
+// in ascending source-rank order (mamba-rs 0.6.2 src/dist/reducer.rs,
+// `DET_SUM_RANKS_SRC` and `reduce_sum_reference`), optionally multiplies by
+// the mean scale with one __fmul_rn (module doc of the same page), and stores.
+// No lane ever combines values of another element, so the bits do not depend
+// on the grid, the vector width or the unroll depth.
+//
+// Modes:
+//   kSumNC        out <- fold(src); sources read through the read-only path
+//                 (out is disjoint from every source).
+//   kSumCoherent  the same with ordinary loads (out may equal one source:
+//                 the in-place fold).
+//   kAllReduce    every arena <- fold(arenas); ordinary loads, then W stores
+//                 (each element is read, then written, by the same thread).
+//
+// Layout: `head` scalar elements until every operand reaches a VEC*4-byte
+// boundary, `nvec` vectors of VEC floats, then a scalar tail. When operands
+// do not share one phase the scalar kernel runs instead (coalesced 4-byte
+// accesses with U*W loads in flight per thread).
+//
+// The small-payload path launches the same kernels with programmatic
+// dependent launch: `griddepcontrol.wait` before the first load (inputs may
+// come from the preceding kernel), `griddepcontrol.launch_dependents` right
+// after, so the next fold's CTAs are resident when this one retires. There
+// are no spin waits of any kind.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace detfold {
+
+enum Mode : int { kSumNC = 0, kSumCoherent = 1, kAllReduce = 2 };
+
+constexpr int kGenericW = 256;  // table capacity of the runtime-W kernels
+
+template <int NT>
+struct FoldParams {
+    const float *src[NT];  // sources (kAllReduce: the arenas, also written)
+    float *out;            // destination of the sum modes
+    int64_t len;           // elements
+    int64_t head;          // scalar elements before the vector body
+    int64_t nvec;          // vectors in the body
+    float scale;           // applied when do_scale != 0
+    int do_scale;
+    int W;                 // runtime world size (used by the generic kernels)
+    int pdl;               // launched with programmatic dependent launch
+};
+
+template <int VEC>
+struct alignas(VEC * 4) Vec {
+    float v[VEC];
+};
+
+// ---------------------------------------------------------------- loads / stores
+
+template <bool NC>
+__device__ __forceinline__ float ld1(const float *p)
+{
+    float x;
+    if constexpr (NC)
+        asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(x) : "l"(p));
+    else
+        asm volatile("ld.global.L1::no_allocate.f32 %0, [%1];" : "=f"(x) : "l"(p) : "memory");
+    return x;
+}
+
+template <int VEC, bool NC>
+__device__ __forceinline__ Vec<VEC> ldv(const float *p)
+{
+    Vec<VEC> r;
+    if constexpr (VEC == 4) {
+        if constexpr (NC)
+            asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3])
+                : "l"(p));
+        else
+            asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3])
+                         : "l"(p)
+                         : "memory");
+    } else {
+        static_assert(VEC == 8, "VEC is 4 or 8");
+        if constexpr (NC)
+            asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
+                  "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+                : "l"(p));
+        else
+            asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]),
+                           "=f"(r.v[4]), "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+                         : "l"(p)
+                         : "memory");
+    }
+    return r;
+}
+
+__device__ __forceinline__ void st1(float *p, float x)
+{
+    asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(x) : "memory");
+}
+
+template <int VEC>
+__device__ __forceinline__ void stv(float *p, const Vec<VEC> &x)
+{
+    if constexpr (VEC == 4)
+        asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(x.v[0]), "f"(x.v[1]),
+                     "f"(x.v[2]), "f"(x.v[3])
+                     : "memory");
+    else
+        asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(x.v[0]),
+                     "f"(x.v[1]), "f"(x.v[2]), "f"(x.v[3]), "f"(x.v[4]), "f"(x.v[5]),
+                     "f"(x.v[6]), "f"(x.v[7])
+                     : "memory");
+}
+
+__device__ __forceinline__ void pdl_enter(int pdl)
+{
+    if (pdl) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+}
+
+// ---------------------------------------------------------------- one element
+
+// The full chain for element i with scalar accesses (head, tail, scalar path).
+template <int W, int MODE, int NT>
+__device__ __forceinline__ void fold_one(const FoldParams<NT> &p, int64_t i)
+{
+    constexpr bool NC = (MODE == kSumNC);
+    const int w = (W > 0) ? W : p.W;
+    float acc = ld1<NC>(p.src[0] + i);
+    if constexpr (W > 0) {
+#pragma unroll
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
+    } else {
+        for (int r = 1; r < w; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
+    }
+    if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+    if constexpr (MODE == kAllReduce) {
+        for (int r = 0; r < w; ++r) st1(const_cast<float *>(p.src[r]) + i, acc);
+    } else {
+        st1(p.out + i, acc);
+    }
+}
+
+template <int VEC, int W, int MODE, int NT>
+__device__ __forceinline__ void store_result(const FoldParams<NT> &p, int64_t e, Vec<VEC> acc)
+{
+    if (p.do_scale) {
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc.v[k] = __fmul_rn(acc.v[k], p.scale);
+    }
+    if constexpr (MODE == kAllReduce) {
+        const int w = (W > 0) ? W : p.W;
+        if constexpr (W > 0) {
+#pragma unroll
+            for (int r = 0; r < W; ++r) stv<VEC>(const_cast<float *>(p.src[r]) + e, acc);
+        } else {
+            for (int r = 0; r < w; ++r) stv<VEC>(const_cast<float *>(p.src[r]) + e, acc);
+        }
+    } else {
+        stv<VEC>(p.out + e, acc);
+    }
+}
+
+// ---------------------------------------------------------------- vector kernel, fixed W
+
+// U vectors per thread per iteration, grid-stride; every operand shares the
+// same VEC*4-byte phase. Element index of vector v is head + v*VEC.
+template <int W, int VEC, int U, int MODE>
+__global__ void __launch_bounds__(256) fold_vec_kernel(const __grid_constant__ FoldParams<W> p)
+{
+    constexpr bool NC = (MODE == kSumNC);
+    pdl_enter(p.pdl);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t v = gtid;
+    for (; v + (U - 1) * stride < p.nvec; v += U * stride) {
+        Vec<VEC> x[U][W];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int r = 0; r < W; ++r)
+                x[u][r] = ldv<VEC, NC>(p.src[r] + p.head + (v + u * stride) * VEC);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            Vec<VEC> acc = x[u][0];
+#pragma unroll
+            for (int r = 1; r < W; ++r)
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) acc.v[k] = __fadd_rn(acc.v[k], x[u][r].v[k]);
+            store_result<VEC, W, MODE>(p, p.head + (v + u * stride) * VEC, acc);
+        }
+    }
+    for (; v < p.nvec; v += stride) {
+        Vec<VEC> x[W];
+#pragma unroll
+        for (int r = 0; r < W; ++r) x[r] = ldv<VEC, NC>(p.src[r] + p.head + v * VEC);
+        Vec<VEC> acc = x[0];
+#pragma unroll
+        for (int r = 1; r < W; ++r)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc.v[k] = __fadd_rn(acc.v[k], x[r].v[k]);
+        store_result<VEC, W, MODE>(p, p.head + v * VEC, acc);
+    }
+    // head and tail: fewer than VEC elements each
+    const int64_t tail0 = p.head + p.nvec * VEC;
+    if (gtid < p.head) fold_one<W, MODE>(p, gtid);
+    if (gtid < p.len - tail0) fold_one<W, MODE>(p, tail0 + gtid);
+}
+
+// ---------------------------------------------------------------- scalar kernel, fixed W
+
+// Operands at different 4-byte phases: coalesced scalar accesses, U elements
+// per thread per iteration with all U*W loads issued first.
+template <int W, int U, int MODE>
+__global__ void __launch_bounds__(256) fold_scalar_kernel(const __grid_constant__ FoldParams<W> p)
+{
+    constexpr bool NC = (MODE == kSumNC);
+    pdl_enter(p.pdl);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (U - 1) * stride < p.len; i += U * stride) {
+        float x[U][W];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int r = 0; r < W; ++r) x[u][r] = ld1<NC>(p.src[r] + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float acc = x[u][0];
+#pragma unroll
+            for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, x[u][r]);
+            if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+            if constexpr (MODE == kAllReduce) {
+#pragma unroll
+                for (int r = 0; r < W; ++r) st1(const_cast<float *>(p.src[r]) + i + u * stride, acc);
+            } else {
+                st1(p.out + i + u * stride, acc);
+            }
+        }
+    }
+    for (; i < p.len; i += stride) fold_one<W, MODE>(p, i);
+}
+
+// ---------------------------------------------------------------- runtime-W kernels (W > 8)
+
+// Loads are issued eight ranks at a time ahead of their adds; the chain
+// order is unchanged.
+template <int VEC, int MODE>
+__global__ void __launch_bounds__(256) fold_vec_generic_kernel(const __grid_constant__ FoldParams<kGenericW> p)
+{
+    constexpr bool NC = (MODE == kSumNC);
+    pdl_enter(p.pdl);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t v = gtid; v < p.nvec; v += stride) {
+        const int64_t e = p.head + v * VEC;
+        Vec<VEC> acc = ldv<VEC, NC>(p.src[0] + e);
+        for (int r0 = 1; r0 < p.W; r0 += 8) {
+            Vec<VEC> x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < p.W) x[k] = ldv<VEC, NC>(p.src[r0 + k] + e);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < p.W)
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) acc.v[j] = __fadd_rn(acc.v[j], x[k].v[j]);
+        }
+        store_result<VEC, 0, MODE>(p, e, acc);
+    }
+    const int64_t tail0 = p.head + p.nvec * VEC;
+    if (gtid < p.head) fold_one<0, MODE>(p, gtid);
+    if (gtid < p.len - tail0) fold_one<0, MODE>(p, tail0 + gtid);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) fold_scalar_generic_kernel(const __grid_constant__ FoldParams<kGenericW> p)
+{
+    constexpr bool NC = (MODE == kSumNC);
+    pdl_enter(p.pdl);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.len; i += stride) {
+        float acc = ld1<NC>(p.src[0] + i);
+        for (int r0 = 1; r0 < p.W; r0 += 8) {
+            float x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < p.W) x[k] = ld1<NC>(p.src[r0 + k] + i);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < p.W) acc = __fadd_rn(acc, x[k]);
+        }
+        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+        if constexpr (MODE == kAllReduce) {
+            for (int r = 0; r < p.W; ++r) st1(const_cast<float *>(p.src[r]) + i, acc);
+        } else {
+            st1(p.out + i, acc);
+        }
+    }
+}
+
+}  // namespace detfold

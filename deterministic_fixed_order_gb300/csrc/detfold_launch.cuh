@@ -1,0 +1,201 @@
+// Host-side launch plumbing shared by the three mode translation units:
+// phase planning (vector width, head, body, tail), grid sizing, and the
+// typed launch of one kernel instantiation.
+#pragma once
+
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "detfold_kernels.cuh"
+
+#ifndef DETFOLD_PREFER_VEC
+#define DETFOLD_PREFER_VEC 4  // 4 = 16-byte vectors, 8 = 32-byte vectors
+#endif
+#ifndef DETFOLD_INFLIGHT_BYTES
+#define DETFOLD_INFLIGHT_BYTES 128  // loaded bytes per thread per unrolled group
+#endif
+#ifndef DETFOLD_SMALL_LEN
+#define DETFOLD_SMALL_LEN (1 << 17)  // elements at or below: small-payload launch
+#endif
+#ifndef DETFOLD_SMALL_THREADS
+#define DETFOLD_SMALL_THREADS 128
+#endif
+#ifndef DETFOLD_BW_THREADS
+#define DETFOLD_BW_THREADS 256
+#endif
+
+namespace detfold {
+
+// One fold launch as the API layer describes it.
+struct LaunchSpec {
+    int W;
+    int mode;                // Mode
+    const float *const *src; // host array of W device pointers
+    float *out;              // sum modes only
+    int64_t len;
+    float scale;
+    int do_scale;
+};
+
+// How the elements are split: `vec` = 8, 4, or 0 for the scalar kernel.
+struct Plan {
+    int vec;
+    int64_t head, nvec;
+};
+
+inline int elem_phase(const void *p, int vec)
+{
+    return (int)(((uintptr_t)p % (uintptr_t)(vec * 4)) / 4);
+}
+
+// The widest vector whose phase every operand shares (the output as well).
+inline Plan make_plan(const LaunchSpec &s)
+{
+    const int prefs[2] = {DETFOLD_PREFER_VEC, 4};
+    for (int k = 0; k < 2; ++k) {
+        const int vec = prefs[k];
+        const int ph = elem_phase(s.src[0], vec);
+        bool same = (s.mode == kAllReduce) || elem_phase(s.out, vec) == ph;
+        for (int r = 1; same && r < s.W; ++r) same = elem_phase(s.src[r], vec) == ph;
+        if (same) {
+            int64_t head = (vec - ph) % vec;
+            if (head > s.len) head = s.len;
+            return Plan{vec, head, (s.len - head) / vec};
+        }
+    }
+    return Plan{0, 0, 0};
+}
+
+inline constexpr int u_for(int W, int vec)
+{
+    // vec == 0: scalar kernel, 4-byte loads
+    return (DETFOLD_INFLIGHT_BYTES / ((vec ? vec : 1) * 4 * W)) > 0
+               ? (DETFOLD_INFLIGHT_BYTES / ((vec ? vec : 1) * 4 * W))
+               : 1;
+}
+
+// Resident CTAs the whole GPU holds for `kernel` at `threads` per CTA,
+// computed once per (instantiation, device).
+template <typename Kernel>
+inline cudaError_t resident_ctas(Kernel kernel, int threads, int *out)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        if (e != cudaSuccess) return e;
+        v = sms * (per_sm > 0 ? per_sm : 1);
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return cudaSuccess;
+}
+
+template <typename Params>
+inline cudaError_t launch_kernel(void (*kernel)(Params), const Params &p, int64_t work, int u,
+                                 bool small, cudaStream_t stream)
+{
+    const int threads = small ? DETFOLD_SMALL_THREADS : DETFOLD_BW_THREADS;
+    int64_t blocks = (work + threads - 1) / threads;
+    if (!small) {
+        const int64_t per_iter = (int64_t)threads * u;
+        blocks = (work + per_iter - 1) / per_iter;
+        int cap = 0;
+        const cudaError_t e = resident_ctas(kernel, threads, &cap);
+        if (e != cudaSuccess) return e;
+        if (blocks > cap) blocks = cap;
+    }
+    if (blocks < 1) blocks = 1;
+    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (small) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <int NT>
+inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool small)
+{
+    FoldParams<NT> p = {};
+    for (int r = 0; r < s.W; ++r) p.src[r] = s.src[r];
+    p.out = s.out;
+    p.len = s.len;
+    p.head = pl.head;
+    p.nvec = pl.nvec;
+    p.scale = s.scale;
+    p.do_scale = s.do_scale;
+    p.W = s.W;
+    p.pdl = small ? 1 : 0;
+    return p;
+}
+
+template <int W, int MODE>
+inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
+{
+    const Plan pl = make_plan(s);
+    const bool small = s.len <= DETFOLD_SMALL_LEN;
+    const FoldParams<W> p = fill_params<W>(s, pl, small);
+    if (pl.vec == 8) {
+        constexpr int U = u_for(W, 8);
+        return launch_kernel(fold_vec_kernel<W, 8, U, MODE>, p, pl.nvec, U, small, stream);
+    }
+    if (pl.vec == 4) {
+        constexpr int U = u_for(W, 4);
+        return launch_kernel(fold_vec_kernel<W, 4, U, MODE>, p, pl.nvec, U, small, stream);
+    }
+    constexpr int U = u_for(W, 0);
+    return launch_kernel(fold_scalar_kernel<W, U, MODE>, p, s.len, U, small, stream);
+}
+
+template <int MODE>
+inline cudaError_t launch_generic(const LaunchSpec &s, cudaStream_t stream)
+{
+    const Plan pl = make_plan(s);
+    const bool small = s.len <= DETFOLD_SMALL_LEN;
+    const FoldParams<kGenericW> p = fill_params<kGenericW>(s, pl, small);
+    if (pl.vec == 8) return launch_kernel(fold_vec_generic_kernel<8, MODE>, p, pl.nvec, 1, small, stream);
+    if (pl.vec == 4) return launch_kernel(fold_vec_generic_kernel<4, MODE>, p, pl.nvec, 1, small, stream);
+    return launch_kernel(fold_scalar_generic_kernel<MODE>, p, s.len, 1, small, stream);
+}
+
+template <int MODE>
+inline cudaError_t launch_mode(const LaunchSpec &s, cudaStream_t stream)
+{
+    switch (s.W) {
+    case 1: return launch_fixed<1, MODE>(s, stream);
+    case 2: return launch_fixed<2, MODE>(s, stream);
+    case 3: return launch_fixed<3, MODE>(s, stream);
+    case 4: return launch_fixed<4, MODE>(s, stream);
+    case 5: return launch_fixed<5, MODE>(s, stream);
+    case 6: return launch_fixed<6, MODE>(s, stream);
+    case 7: return launch_fixed<7, MODE>(s, stream);
+    case 8: return launch_fixed<8, MODE>(s, stream);
+    default: return launch_generic<MODE>(s, stream);
+    }
+}
+
+// Defined one per translation unit (fold_sum_nc.cu, fold_sum_coherent.cu,
+// fold_allreduce.cu) so the instantiations compile in parallel.
+cudaError_t launch_sum_nc(const LaunchSpec &s, cudaStream_t stream);
+cudaError_t launch_sum_coherent(const LaunchSpec &s, cudaStream_t stream);
+cudaError_t launch_allreduce(const LaunchSpec &s, cudaStream_t stream);
+cudaError_t launch_empty(int count, int pdl, cudaStream_t stream);
+
+}  // namespace detfold

@@ -1,0 +1,62 @@
+"""Run one fold row at a chosen size for a few launches (for profiler captures).
+
+    python -m deterministic_fixed_order_gb300.profile_case ROW --len N [--W W] [--launches K]
+
+ROW is one of: stacked, ptrs, allreduce, staged, scale, small. Inputs are
+seeded synthetic data. Parity of these calls is established by the test
+suite; this runner only launches them and reports the status.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("row", choices=["stacked", "ptrs", "allreduce", "staged", "scale", "small"])
+    ap.add_argument("--len", type=int, required=True)
+    ap.add_argument("--W", type=int, default=8)
+    ap.add_argument("--launches", type=int, default=3)
+    a = ap.parse_args()
+
+    import torch
+
+    import deterministic_fixed_order_gb300 as df
+    import detfold_inputs as gen
+
+    dev = torch.device("cuda:0")
+    W, n = a.W, a.len
+    rows = gen.gradient_rows(W, n)
+    d = torch.from_numpy(rows).to(dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    if a.row in ("stacked", "small"):
+        fn = lambda: df.detfold_sum_stacked(out, d, W, n)
+    elif a.row == "ptrs":
+        srcs = [d[r] for r in range(W)]
+        fn = lambda: df.detfold_sum_ptrs(out, srcs, W, n)
+    elif a.row == "scale":
+        out.copy_(d[0])
+        fn = lambda: df.detfold_scale(out, n, 0.5)
+    else:
+        arenas = [d[r] for r in range(W)]
+        if a.row == "allreduce":
+            fn = lambda: df.detfold_loopback_allreduce(arenas, W, n, 0.25)
+        else:
+            nb = df.detfold_staged_workspace_bytes(n, W)
+            ws = torch.empty(nb // 4, dtype=torch.float32, device=dev)
+            fn = lambda: df.detfold_loopback_allreduce_staged(arenas, W, n, 0.25, 0, ws, nb)
+    for _ in range(a.launches):
+        fn()
+    torch.cuda.synchronize()
+    print(f"profile_case {a.row} W={W} len={n}: {a.launches} launches ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

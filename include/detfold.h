@@ -1,0 +1,173 @@
+/*
+ * libdetfold -- fixed-order elementwise fold for GB300 (sm_103a).
+ *
+ * What is computed (mamba-rs 0.6.2 src/dist/reducer.rs, module doc and
+ * `reduce_sum_reference`): for W rank addends s_0..s_{W-1} of an f32 arena,
+ *
+ *     out[i] = ((s_0[i] + s_1[i]) + s_2[i]) + ... + s_{W-1}[i]
+ *
+ * a serial IEEE binary32 round-to-nearest-even add chain in strictly
+ * ascending source-rank order, starting from s_0[i] (so an all -0 column
+ * stays -0). Subnormals are kept (no flush to zero). The bits therefore do
+ * not depend on the launch shape, the transport or the delivery order. The
+ * optional mean is a separate multiply, out[i] = fl(sum[i] * mean_scale),
+ * with mean_scale normally fl(1/W), which is exact for power-of-two W
+ * unless the product underflows.
+ *
+ * Conventions shared by every entry point:
+ *   - Return value: DETFOLD_OK (0) or a negative DETFOLD_ERR_* code. No
+ *     entry point aborts, prints, synchronizes or allocates device memory.
+ *     On any error nothing has been enqueued, except DETFOLD_ERR_CUDA from
+ *     a multi-launch call, where earlier launches may already be enqueued.
+ *   - Pointers named "device" are caller-owned device memory of the current
+ *     device (for example torch tensors); the library keeps no reference
+ *     after the call returns. They must be 4-byte aligned; any 4-byte
+ *     phase is legal (vector loads are used where every operand shares
+ *     the same 16- or 32-byte phase, scalar loads otherwise).
+ *   - Arrays named "host" (pointer tables, shard-plan outputs) are read or
+ *     written only during the call. Pointer tables are copied into kernel
+ *     parameters, so a captured CUDA graph keeps the addresses it saw.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). All device work is stream-ordered and asynchronous.
+ *   - len is an element count (f32 words); len == 0 is a no-op returning
+ *     DETFOLD_OK once the pointer and W arguments have been checked
+ *     (mamba-rs src/dist/reducer.rs `DetReduceKernel::launch`, `copy_d2d`).
+ *   - W (the world size) must be 1 <= W <= DETFOLD_MAX_W
+ *     (`reduce_sum_reference` asserts a non-empty world).
+ */
+#ifndef DETFOLD_H
+#define DETFOLD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DETFOLD_MAX_W 256
+/* Largest accepted len: 2^40 elements (4 TiB per addend). */
+#define DETFOLD_MAX_LEN ((int64_t)1 << 40)
+
+/* Status codes. */
+#define DETFOLD_OK 0
+#define DETFOLD_ERR_NULL (-1)      /* a required pointer is NULL                    */
+#define DETFOLD_ERR_WORLD (-2)     /* W < 1 or W > DETFOLD_MAX_W                    */
+#define DETFOLD_ERR_LEN (-3)       /* len < 0 or len > DETFOLD_MAX_LEN               */
+#define DETFOLD_ERR_ALIGN (-4)     /* a device pointer is not 4-byte aligned         */
+#define DETFOLD_ERR_OVERLAP (-5)   /* operands overlap in a way the call forbids     */
+#define DETFOLD_ERR_WORKSPACE (-6) /* workspace missing, too small or misaligned     */
+#define DETFOLD_ERR_CUDA (-7)      /* a CUDA call failed; see detfold_last_cuda_error */
+#define DETFOLD_ERR_ARG (-8)       /* another invalid argument (unknown flag bits)   */
+
+/* Flags of detfold_loopback_allreduce_staged. */
+#define DETFOLD_STAGED_REVERSE_DELIVERY 1 /* copy peers into the stack in descending rank order */
+#define DETFOLD_STAGED_SEPARATE_SCALE 2   /* mean multiply as its own pass, not in the fold store */
+
+/*
+ * Stacked fold (mamba-rs src/dist/reducer.rs, `DET_SUM_RANKS_SRC` and
+ * `DetReduceKernel::launch`).
+ *   out     device, len f32, written.
+ *   stacked device, row-major [W][len] f32, slot (row) r = source rank r, read.
+ *   out must not overlap stacked (DETFOLD_ERR_OVERLAP).
+ * W == 1 copies row 0 into out.
+ */
+int detfold_sum_stacked(float *out, const float *stacked, int W, int64_t len, void *stream);
+
+/*
+ * Pointer-table fold: the same chain over W independent arenas, without the
+ * copy into a stacked buffer that the reference's `LoopbackWorld::run_round`
+ * makes (mamba-rs src/dist/reducer.rs) -- the kernel reads every rank's
+ * arena directly.
+ *   out  device, len f32, written. It may be exactly one of the sources
+ *        (out == srcs[k], the in-place fold of memra-engine 0.128.0
+ *        tests/tp_ar_gpu.rs `memra_tp_ar_fold(dst, stage, ...)`); any other
+ *        overlap with a source is DETFOLD_ERR_OVERLAP. Sources may overlap
+ *        each other (they are only read).
+ *   srcs host array of W device pointers, each to len f32, read.
+ */
+int detfold_sum_ptrs(float *out, const float *const *srcs, int W, int64_t len, void *stream);
+
+/*
+ * The mean as its own pass (mamba-rs src/dist/reducer.rs, module doc: the
+ * caller multiplies the sum by 1/W): buf[i] = fl(buf[i] * scale), in place.
+ *   buf device, len f32, read and written.
+ * scale == 1.0f enqueues nothing.
+ */
+int detfold_scale(float *buf, int64_t len, float scale, void *stream);
+
+/*
+ * Fused loopback all-reduce, in place: for each i, read arenas[0..W-1][i],
+ * fold in ascending rank order, multiply by mean_scale (skipped when it is
+ * exactly 1.0f), and write the result to every arena. One pass replaces the
+ * reference's exchange + fold + distribute (mamba-rs src/dist/reducer.rs,
+ * `LoopbackWorld::run_round`, `reduce_sum_fixed_order_nccl`); the end state
+ * is the same: every arena holds the identical ascending-rank sum.
+ *   arenas host array of W device pointers, each to len f32, read and
+ *          written. Arenas must be pairwise disjoint (DETFOLD_ERR_OVERLAP).
+ * W == 1 leaves the arena as it is except for the mean multiply.
+ */
+int detfold_loopback_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
+                               void *stream);
+
+/*
+ * Bytes of device workspace that detfold_loopback_allreduce_staged needs
+ * for (len, W): W stack rows of the largest owner shard, padded so that
+ * every row can share its source shard's 32-byte phase. Returns a negative
+ * status for invalid len or W.
+ */
+int64_t detfold_staged_workspace_bytes(int64_t len, int W);
+
+/*
+ * Staged loopback all-reduce: the reference's own dataflow on one device
+ * (mamba-rs src/dist/reducer.rs, `LoopbackWorld::run_round`), kept as the
+ * comparator of the fused call. For each owner o with a non-empty shard
+ * (detfold_shard_plan): copy every rank's slice of that shard into stack
+ * slot = source rank (device-to-device copies, ascending rank order, or
+ * descending with DETFOLD_STAGED_REVERSE_DELIVERY -- the bits must not
+ * change), fold the slots into arena o's shard, and apply mean_scale in the
+ * fold's store (or as a separate pass with DETFOLD_STAGED_SEPARATE_SCALE).
+ * Then copy every owner's shard to all other arenas. Same end state and
+ * bits as detfold_loopback_allreduce.
+ *   arenas    host array of W device pointers (as above, pairwise disjoint).
+ *   workspace device, >= detfold_staged_workspace_bytes(len, W) bytes,
+ *             16-byte aligned, disjoint from every arena; contents on entry
+ *             are ignored, on return undefined. Not needed when W == 1.
+ * Unlike the reference, no stream synchronization happens between owners:
+ * the workspace is caller-owned, so stream order alone protects its reuse.
+ */
+int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
+                                      float mean_scale, int flags, void *workspace,
+                                      int64_t workspace_bytes, void *stream);
+
+/*
+ * Contiguous owner shards (imported as `shard_plan` by mamba-rs
+ * src/dist/reducer.rs; its body is not printed there). Reading: balanced,
+ * shard r = {start = r*base + min(r, rem), len = base + (r < rem)} with
+ * base = len / W, rem = len % W; shards may be empty when len < W.
+ *   starts, lens  host arrays of W int64, written.
+ * Host only; touches no device.
+ */
+int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens);
+
+/* A static, human-readable name for a status code. */
+const char *detfold_status_string(int status);
+
+/*
+ * The cudaError_t value of the last DETFOLD_ERR_CUDA returned on the calling
+ * thread (0 if none).
+ */
+int detfold_last_cuda_error(void);
+
+/*
+ * Launch-latency floor probe: enqueues `count` launches of an empty kernel
+ * (one CTA of 32 threads) on `stream`, with programmatic dependent launch
+ * when pdl != 0, exactly as the small-payload fold path launches. Used to
+ * measure the floor that a graph of small folds is compared against.
+ */
+int detfold_launch_floor(int count, int pdl, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DETFOLD_H */

@@ -1,0 +1,206 @@
+"""The C-ABI boundary on the CPU: the library loads, exports every declared
+symbol, and its host logic (argument validation, the shard plan, status
+strings) behaves as include/detfold.h states. No call here reaches a kernel
+launch, except the no-device check, which only runs where no GPU exists.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from deterministic_fixed_order_gb300 import build as dbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "detfold.h")
+
+
+@pytest.fixture(scope="module")
+def df():
+    dbuild.build()
+    import deterministic_fixed_order_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(detfold_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for want in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
+                 "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
+                 "detfold_staged_workspace_bytes", "detfold_shard_plan",
+                 "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(df):
+    out = subprocess.run(["nm", "-D", "--defined-only", df.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (detfold_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        getattr(df.lib, n)  # resolvable through ctypes
+
+
+def test_header_compiles_as_c():
+    src = '#include "detfold.h"\nint main(void){return DETFOLD_OK;}\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-", "-o", os.devnull], input=src, text=True,
+                       capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings(df):
+    for name, code in df.STATUS.items():
+        s = df.detfold_status_string(code)
+        assert s and s != "unknown status", name
+    assert df.detfold_status_string(12345) == "unknown status"
+
+
+def test_shard_plan_matches_oracle(df):
+    for W in range(1, 12):
+        for n in list(range(0, 40)) + [1000003, 100_000_000, (1 << 20) + 7]:
+            s, l = df.detfold_shard_plan(n, W)
+            os_, ol = oracle.shard_plan(n, W)
+            assert s == list(os_) and l == list(ol)
+
+
+def test_shard_plan_errors(df):
+    L = df.lib
+    buf = (ctypes.c_int64 * 4)()
+    assert L.detfold_shard_plan(10, 0, buf, buf) == df.STATUS["DETFOLD_ERR_WORLD"]
+    assert L.detfold_shard_plan(10, 257, buf, buf) == df.STATUS["DETFOLD_ERR_WORLD"]
+    assert L.detfold_shard_plan(-1, 4, buf, buf) == df.STATUS["DETFOLD_ERR_LEN"]
+    assert L.detfold_shard_plan(10, 4, None, buf) == df.STATUS["DETFOLD_ERR_NULL"]
+
+
+def test_workspace_bytes(df):
+    for n, W in ((100_000_000, 4), ((1 << 20) + 7, 3), (5, 8), (0, 2)):
+        b = df.detfold_staged_workspace_bytes(n, W)
+        shard = -(-n // W)
+        assert b >= W * (shard + 8) * 4 and b % 4 == 0
+    assert df.lib.detfold_staged_workspace_bytes(10, 0) == df.STATUS["DETFOLD_ERR_WORLD"]
+    assert df.lib.detfold_staged_workspace_bytes(-3, 2) == df.STATUS["DETFOLD_ERR_LEN"]
+
+
+# Fake device addresses: validation rejects these calls before any launch.
+A = 1 << 32
+
+
+def _tab(*ptrs):
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+def test_validation_sum_stacked(df):
+    L, S = df.lib, df.STATUS
+    assert L.detfold_sum_stacked(None, A, 2, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_sum_stacked(A, None, 2, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_sum_stacked(A, A + 4096, 0, 8, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_sum_stacked(A, A + 4096, 257, 8, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_sum_stacked(A, A + 4096, 2, -1, None) == S["DETFOLD_ERR_LEN"]
+    assert L.detfold_sum_stacked(A, A + 4096, 2, (1 << 40) + 1, None) == S["DETFOLD_ERR_LEN"]
+    assert L.detfold_sum_stacked(A + 2, A + 4096, 2, 8, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_sum_stacked(A, A + 4098, 2, 8, None) == S["DETFOLD_ERR_ALIGN"]
+    # out inside the stacked rows, or overlapping their start
+    assert L.detfold_sum_stacked(A + 32, A, 2, 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_sum_stacked(A, A + 28, 2, 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    # len == 0: a no-op once pointers and W are valid
+    assert L.detfold_sum_stacked(A, A, 2, 0, None) == S["DETFOLD_OK"]
+
+
+def test_validation_sum_ptrs(df):
+    L, S = df.lib, df.STATUS
+    assert L.detfold_sum_ptrs(A, None, 2, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_sum_ptrs(A, _tab(A + 4096, 0), 2, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_sum_ptrs(A, _tab(A + 4096, A + 8192), 0, 8, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_sum_ptrs(A, _tab(A + 4096, A + 8194), 2, 8, None) == S["DETFOLD_ERR_ALIGN"]
+    # out partially overlapping a source is refused; out == a source is the in-place fold
+    assert L.detfold_sum_ptrs(A, _tab(A + 4, A + 8192), 2, 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_sum_ptrs(A, _tab(A, A + 8192), 2, 0, None) == S["DETFOLD_OK"]
+    # W == 1 in place: nothing to do, nothing launched
+    assert L.detfold_sum_ptrs(A, _tab(A), 1, 8, None) == S["DETFOLD_OK"]
+
+
+def test_validation_allreduce(df):
+    L, S = df.lib, df.STATUS
+    assert L.detfold_loopback_allreduce(None, 2, 8, 1.0, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_loopback_allreduce(_tab(A, 0), 2, 8, 1.0, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_loopback_allreduce(_tab(A, A + 4096), 300, 8, 1.0, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_loopback_allreduce(_tab(A, A + 4097), 2, 8, 1.0, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_loopback_allreduce(_tab(A, A), 2, 8, 1.0, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_loopback_allreduce(_tab(A, A + 16), 2, 8, 1.0, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_loopback_allreduce(_tab(A, A + 4096), 2, 0, 0.5, None) == S["DETFOLD_OK"]
+    # one rank, scale 1: nothing to do
+    assert L.detfold_loopback_allreduce(_tab(A), 1, 8, 1.0, None) == S["DETFOLD_OK"]
+
+
+def test_validation_staged(df):
+    L, S = df.lib, df.STATUS
+    ws_need = df.detfold_staged_workspace_bytes(64, 2)
+    arenas = _tab(A, A + 4096)
+    W_ = A + (1 << 20)
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 4, W_, ws_need, None) == S["DETFOLD_ERR_ARG"]
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, None, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, W_, ws_need - 4, None) == S["DETFOLD_ERR_WORKSPACE"]
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, W_ + 8, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, A + 64, ws_need, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_loopback_allreduce_staged(_tab(A, A), 2, 64, 1.0, 0, W_, ws_need, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 0, 0.5, 0, None, 0, None) == S["DETFOLD_OK"]
+
+
+def test_validation_scale_and_floor(df):
+    L, S = df.lib, df.STATUS
+    assert L.detfold_scale(None, 8, 0.5, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_scale(A + 1, 8, 0.5, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_scale(A, -8, 0.5, None) == S["DETFOLD_ERR_LEN"]
+    assert L.detfold_scale(A, 8, 1.0, None) == S["DETFOLD_OK"]   # scale 1: nothing enqueued
+    assert L.detfold_launch_floor(-1, 1, None) == S["DETFOLD_ERR_ARG"]
+    assert L.detfold_launch_floor(0, 1, None) == S["DETFOLD_OK"]
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return True  # unknown: assume a GPU and skip
+
+
+@pytest.mark.skipif(_has_gpu() or os.path.exists("/dev/nvidia0"),
+                    reason="only meaningful (and only safe) where no GPU exists")
+def test_launch_without_device_reports_cuda_error(df):
+    L, S = df.lib, df.STATUS
+    rc = L.detfold_sum_stacked(A, A + 4096, 2, 8, None)
+    assert rc == S["DETFOLD_ERR_CUDA"]
+    assert L.detfold_last_cuda_error() != 0
+    with pytest.raises(df.DetfoldError):
+        df.detfold_sum_stacked(A, A + 4096, 2, 8, stream=0)
+
+
+def test_binding_checks_tensor_sizes(df):
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(8)
+    with pytest.raises(TypeError):
+        df.detfold_sum_stacked(t, t, 2, 4, stream=0)   # CPU tensors are refused
+
+
+def test_oracle_and_library_share_no_code():
+    # Neither side includes, imports or links the other.
+    pkg = os.path.join(ROOT, "deterministic_fixed_order_gb300")
+    banned = re.compile(r"^\s*(import\s+oracle|from\s+oracle|#include\s+.*oracle)", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                assert not banned.search(open(os.path.join(dirpath, f)).read()), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "deterministic_fixed_order_gb300" not in text and "detfold.h" not in text, f

@@ -1,0 +1,358 @@
+"""GPU parity: the CUDA library against the CPU oracle, bit for bit (0 ULP).
+
+Fold and mean: mamba-rs 0.6.2 src/dist/reducer.rs (module doc,
+`reduce_sum_reference`, `LoopbackWorld::run_round`). Gate patterns: memra-engine
+0.128.0 tests/tp_ar_gpu.rs (sizes 1..65536, repeat call gives 2S, red arm) and
+memra-engine 0.136.0 tests/gdn_packed_gpu.rs (graph replay with rebinding).
+Every device buffer has sentinel guard bands that must survive each call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import detfold_inputs as gen
+import oracle
+from gpu_util import Guarded, assert_bitwise, nonvacuous
+
+import deterministic_fixed_order_gb300 as df
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+C1_SIZES = [1, 4, 1024, 4096, 16384, 65536]
+C5_LEN = (1 << 20) + 7
+
+
+def sync():
+    torch.cuda.synchronize()
+
+
+def run_stacked(rows: np.ndarray, offset: int = 0, out_offset: int | None = None):
+    W, n = rows.shape
+    st = Guarded(W * n, offset, rows)
+    out = Guarded(n, offset if out_offset is None else out_offset)
+    df.detfold_sum_stacked(out.t, st.t, W, n)
+    sync()
+    assert st.intact() and out.intact(), "guard band overwritten"
+    return out.host()
+
+
+def run_ptrs(rows: np.ndarray, offsets=None, out_offset: int = 0):
+    W, n = rows.shape
+    offsets = offsets or [0] * W
+    srcs = [Guarded(n, offsets[r], rows[r]) for r in range(W)]
+    out = Guarded(n, out_offset)
+    df.detfold_sum_ptrs(out.t, [s.t for s in srcs], W, n)
+    sync()
+    assert all(s.intact() for s in srcs) and out.intact(), "guard band overwritten"
+    for r in range(W):
+        assert_bitwise(srcs[r].host(), rows[r], f"source {r} modified")
+    return out.host()
+
+
+def run_allreduce(rows: np.ndarray, scale: float = 1.0, offsets=None, staged_flags=None):
+    W, n = rows.shape
+    offsets = offsets or [0] * W
+    arenas = [Guarded(n, offsets[r], rows[r]) for r in range(W)]
+    if staged_flags is None:
+        df.detfold_loopback_allreduce([a.t for a in arenas], W, n, scale)
+    else:
+        nb = df.detfold_staged_workspace_bytes(n, W)
+        ws = torch.empty(max(1, nb // 4), dtype=torch.float32, device="cuda")
+        df.detfold_loopback_allreduce_staged([a.t for a in arenas], W, n, scale, staged_flags,
+                                             ws, nb)
+    sync()
+    assert all(a.intact() for a in arenas), "guard band overwritten"
+    return [a.host() for a in arenas]
+
+
+def oracle_allreduce(rows: np.ndarray, scale: float = 1.0):
+    arenas = [rows[r].copy() for r in range(rows.shape[0])]
+    oracle.allreduce(arenas, np.float32(scale))
+    return arenas
+
+
+# ------------------------------------------------------------------ C1: W = 2 decode-join sizes
+
+@pytest.mark.parametrize("n", C1_SIZES)
+def test_c1_stacked_bitwise_and_repeat_call(n):
+    rows = gen.c1_rows(2, n)
+    want = oracle.fold_stacked(rows)
+    got = run_stacked(rows)
+    assert_bitwise(got, want, f"C1 n={n}")
+    nz, am = nonvacuous(got)
+    assert nz > 0 and am > 0
+    # Repeat call: both rows now hold S (as after an all-reduce): exactly 2S.
+    again = run_stacked(np.stack([got, got]))
+    assert_bitwise(again, oracle.fold(np.stack([want, want])), f"C1 repeat n={n}")
+    assert np.array_equal(again.astype(np.float64), 2.0 * want.astype(np.float64))
+
+
+@pytest.mark.parametrize("n", C1_SIZES)
+def test_c1_ptrs_and_allreduce_forms(n):
+    rows = gen.c1_rows(2, n)
+    want = oracle.fold(rows)
+    assert_bitwise(run_ptrs(rows), want, f"C1 ptrs n={n}")
+    arenas = [Guarded(n, 0, rows[r]) for r in range(2)]
+    for call in range(2):
+        df.detfold_loopback_allreduce([a.t for a in arenas], 2, n, 1.0)
+        sync()
+        exp = want if call == 0 else oracle.fold(np.stack([want, want]))
+        for r in range(2):
+            assert_bitwise(arenas[r].host(), exp, f"C1 all-reduce n={n} call={call} rank={r}")
+        assert all(a.intact() for a in arenas)
+
+
+def test_red_arm_fold_without_peer_contribution_diverges():
+    # In-place fold with a zero stage: rank 0 keeps its own partial, which
+    # must not reproduce the sum (else the bitwise gate proves nothing).
+    n = 4096
+    a, b = gen.vecf(n, 5), gen.vecf(n, 6)
+    dst = Guarded(n, 0, a)
+    stage = Guarded(n, 0, np.zeros(n, np.float32))
+    df.detfold_sum_ptrs(dst.t, [dst.t, stage.t], 2, n)
+    sync()
+    got = dst.host()
+    want = oracle.fold(np.stack([a, b]))
+    same = int(np.count_nonzero(got.view(np.uint32) == want.view(np.uint32)))
+    assert same < n
+    assert_bitwise(got, a, "fold with zero stage")
+
+
+# ------------------------------------------------------------------ heads, tails, phases
+
+@pytest.mark.parametrize("W", [1, 2, 3, 5, 8])
+def test_every_small_length_and_head_offset(W):
+    rows_all = gen.stress_rows(W, 64)
+    for n in range(1, 65):
+        rows = np.ascontiguousarray(rows_all[:, :n])
+        want = oracle.fold(rows)
+        for off in range(8):
+            assert_bitwise(run_ptrs(rows, [off] * W, off), want, f"ptrs W={W} n={n} off={off}")
+        for off in (0, 1, 3, 5):
+            assert_bitwise(run_stacked(rows, off), want, f"stacked W={W} n={n} off={off}")
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 6, 7, 8, 9, 16])
+@pytest.mark.parametrize("n", [1, 7, 1000, 4099, C5_LEN])
+def test_mismatched_phases(W, n):
+    rows = gen.stress_rows(W, n)
+    want = oracle.fold(rows)
+    offs = [(r * 3) % 8 for r in range(W)]
+    assert_bitwise(run_ptrs(rows, offs, out_offset=5), want, f"ptrs W={W} n={n}")
+    got = run_allreduce(rows, float(oracle.mean_scale(W)), offs)
+    exp = oracle_allreduce(rows, oracle.mean_scale(W))
+    for r in range(W):
+        assert_bitwise(got[r], exp[r], f"all-reduce W={W} n={n} rank={r}")
+
+
+# ------------------------------------------------------------------ C5: odd worlds, stress values
+
+@pytest.mark.parametrize("W", [3, 6])
+@pytest.mark.parametrize("variant", ["base+4", "per-rank-phase"])
+def test_c5_stress_sum_mean_and_allreduce(W, variant):
+    rows = gen.stress_rows(W, C5_LEN)
+    s_want = oracle.fold(rows)
+    m = oracle.mean_scale(W)
+    mean_want = oracle.scale(s_want, m)
+    offs = [1] * W if variant == "base+4" else [r % 4 for r in range(W)]
+    if variant == "base+4":
+        assert_bitwise(run_stacked(rows, 1, 1), s_want, f"C5 stacked W={W}")
+    got = run_ptrs(rows, offs, out_offset=1)
+    assert_bitwise(got, s_want, f"C5 ptrs W={W} {variant}")
+    # the mean as its own pass over the sum
+    buf = Guarded(C5_LEN, 1, got)
+    df.detfold_scale(buf.t, C5_LEN, float(m))
+    sync()
+    assert buf.intact()
+    assert_bitwise(buf.host(), mean_want, f"C5 mean W={W}")
+    # fused all-reduce with the mean in registers, and the staged comparator
+    for flags in (None, 0, 1, 2, 3):
+        ar = run_allreduce(rows, float(m), offs, staged_flags=flags)
+        for r in range(W):
+            assert_bitwise(ar[r], mean_want, f"C5 all-reduce W={W} flags={flags} rank={r}")
+    nz, am = nonvacuous(s_want)
+    assert nz > 0 and am > 0
+
+
+def test_c5_special_columns():
+    # Elements 0..15 of the stress rows hold signed-zero, subnormal,
+    # cancellation and order-sensitive columns (see detfold_inputs/gen.c).
+    for W in (3, 6):
+        rows = np.ascontiguousarray(gen.stress_rows(W, 64)[:, :16])
+        want = oracle.fold(rows)
+        assert_bitwise(run_ptrs(rows), want, f"specials W={W}")
+        assert want.view(np.uint32)[0] == 0x80000000  # all -0 stays -0
+
+
+# ------------------------------------------------------------------ runtime-W kernels
+
+@pytest.mark.parametrize("W", [9, 16, 33, 256])
+@pytest.mark.parametrize("n", [1, 1000, 4099, (1 << 17) + 3])
+def test_generic_world_sizes(W, n):
+    rows = gen.normal_rows(W, n)
+    want = oracle.fold(rows)
+    assert_bitwise(run_stacked(rows), want, f"generic stacked W={W} n={n}")
+    assert_bitwise(run_ptrs(rows), want, f"generic ptrs W={W} n={n}")
+    got = run_allreduce(rows, 0.5)
+    exp = oracle_allreduce(rows, 0.5)
+    for r in (0, W - 1):
+        assert_bitwise(got[r], exp[r], f"generic all-reduce W={W} n={n}")
+
+
+@pytest.mark.parametrize("W", [2, 4, 8])
+@pytest.mark.parametrize("k", ["first", "last"])
+@pytest.mark.parametrize("n", [4099, C5_LEN])
+def test_in_place_fold(W, k, n):
+    rows = gen.gradient_rows(W, n)
+    want = oracle.fold(rows)
+    srcs = [Guarded(n, 0, rows[r]) for r in range(W)]
+    kk = 0 if k == "first" else W - 1
+    df.detfold_sum_ptrs(srcs[kk].t, [s.t for s in srcs], W, n)
+    sync()
+    assert all(s.intact() for s in srcs)
+    assert_bitwise(srcs[kk].host(), want, f"in place W={W} k={k}")
+
+
+# ------------------------------------------------------------------ all-reduce: fused vs staged
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 6, 8])
+@pytest.mark.parametrize("n", [1, 5, 7, 4099, 100_003])
+def test_allreduce_fused_and_staged_match_oracle(W, n):
+    rows = gen.normal_rows(W, n)
+    for scale in (1.0, float(oracle.mean_scale(W))):
+        exp = oracle_allreduce(rows, scale)
+        for flags in (None, 0, 1, 2, 3):
+            got = run_allreduce(rows, scale, staged_flags=flags)
+            for r in range(W):
+                assert_bitwise(got[r], exp[r], f"W={W} n={n} scale={scale} flags={flags} r={r}")
+
+
+def test_allreduce_repeat_call_matches_oracle_on_updated_state():
+    n = 65536 + 3
+    for W in (2, 4, 6):
+        rows = gen.normal_rows(W, n)
+        arenas = [Guarded(n, 0, rows[r]) for r in range(W)]
+        host = [rows[r].copy() for r in range(W)]
+        for call in range(3):
+            df.detfold_loopback_allreduce([a.t for a in arenas], W, n, 1.0)
+            oracle.allreduce(host)
+            sync()
+            for r in range(W):
+                assert_bitwise(arenas[r].host(), host[r], f"W={W} call={call} rank={r}")
+
+
+def test_len_zero_and_one_rank_are_noops():
+    a = Guarded(16, 0, np.arange(16, dtype=np.float32))
+    df.detfold_loopback_allreduce([a.t], 1, 16, 1.0)
+    df.detfold_sum_ptrs(a.t, [a.t], 1, 16)
+    df.detfold_scale(a.t, 16, 1.0)
+    df.detfold_loopback_allreduce([a.t], 1, 0, 0.5)
+    sync()
+    assert_bitwise(a.host(), np.arange(16, dtype=np.float32), "no-op calls changed data")
+    assert a.intact()
+
+
+# ------------------------------------------------------------------ C2: small payload + graphs
+
+@pytest.mark.parametrize("n", [4096, 65536])
+def test_c2_small_path_and_graph_replay(n):
+    rows = gen.c1_rows(2, n)
+    want = oracle.fold(rows)
+    st = Guarded(2 * n, 0, rows)
+    out = Guarded(n)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        df.detfold_sum_stacked(out.t, st.t, 2, n)  # warm up outside capture
+    stream.synchronize()
+    out.t.zero_()
+    sync()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(200):
+            df.detfold_sum_stacked(out.t, st.t, 2, n)
+    for _ in range(3):
+        g.replay()
+    sync()
+    assert out.intact() and st.intact()
+    assert_bitwise(out.host(), want, f"graph replay n={n}")
+
+
+def test_graph_recapture_with_rebound_buffers():
+    # The pointer table is baked in at capture: a second capture over new
+    # buffers (the canonical/alternate swap of the graph-rebind gate) must
+    # give the same bits on its own inputs.
+    n = 4096
+    rows = gen.c1_rows(2, n)
+    want = oracle.fold(rows)
+    bufs = [(Guarded(n, 0, rows[0]), Guarded(n, 0, rows[1]), Guarded(n)) for _ in range(2)]
+    graphs = []
+    stream = torch.cuda.Stream()
+    for a, b, o in bufs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(50):
+                df.detfold_sum_ptrs(o.t, [a.t, b.t], 2, n)
+        graphs.append(g)
+    for order in ((0, 1), (1, 0)):
+        for k in order:
+            bufs[k][2].t.zero_()
+            graphs[k].replay()
+        sync()
+        for a, b, o in bufs:
+            assert_bitwise(o.host(), want, "recaptured graph")
+            assert o.intact()
+
+
+def test_many_back_to_back_small_folds_on_a_stream():
+    n = 4096
+    rows = gen.c1_rows(2, n)
+    want = oracle.fold(rows)
+    st = Guarded(2 * n, 0, rows)
+    out = Guarded(n)
+    for _ in range(2000):
+        df.detfold_sum_stacked(out.t, st.t, 2, n)
+    sync()
+    assert_bitwise(out.host(), want, "2000 back-to-back folds")
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.slow
+def test_c3_full_size_w8_gradient_bitwise():
+    W, n = 8, 1 << 26
+    rows = gen.gradient_rows(W, n)
+    want = oracle.fold_stacked(rows)
+    st = torch.from_numpy(rows).cuda()
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    df.detfold_sum_stacked(out, st, W, n)
+    sync()
+    assert_bitwise(out.cpu().numpy(), want, "C3 stacked")
+    out.zero_()
+    df.detfold_sum_ptrs(out, [st[r] for r in range(W)], W, n)
+    sync()
+    assert_bitwise(out.cpu().numpy(), want, "C3 ptrs")
+    nz, am = nonvacuous(want)
+    assert nz > 0.99 * n and am > 1.0
+
+
+@pytest.mark.slow
+def test_c4_full_size_w4_fused_and_staged_bitwise():
+    W, n = 4, 100_000_000
+    rows = gen.normal_rows(W, n)
+    exp = oracle_allreduce(rows, 0.25)
+    fused = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
+    df.detfold_loopback_allreduce(fused, W, n, 0.25)
+    sync()
+    for r in range(W):
+        assert_bitwise(fused[r].cpu().numpy(), exp[r], f"C4 fused rank {r}")
+    del fused
+    nb = df.detfold_staged_workspace_bytes(n, W)
+    ws = torch.empty(nb // 4, dtype=torch.float32, device="cuda")
+    for flags in (0, df.DETFOLD_STAGED_SEPARATE_SCALE | df.DETFOLD_STAGED_REVERSE_DELIVERY):
+        staged = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
+        df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, flags, ws, nb)
+        sync()
+        for r in range(W):
+            assert_bitwise(staged[r].cpu().numpy(), exp[r], f"C4 staged flags={flags} rank {r}")
+        del staged

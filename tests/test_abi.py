@@ -12,7 +12,6 @@ import numpy as np
 import pytest
 
 import oracle
-from deterministic_fixed_order_gb300 import build as dbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "detfold.h")
@@ -20,7 +19,6 @@ HEADER = os.path.join(ROOT, "include", "detfold.h")
 
 @pytest.fixture(scope="module")
 def df():
-    dbuild.build()
     import deterministic_fixed_order_gb300 as m
     return m
 

@@ -61,13 +61,17 @@ GRAPH_NODES = 10_000
 NCU_TRAFFIC = {}
 
 
+KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "fold_sum_nc.cu",
+                "fold_sum_coherent.cu", "fold_allreduce.cu")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the fold kernels and their launch configuration."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "deterministic_fixed_order_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in KERNEL_FILES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 

@@ -24,8 +24,8 @@ __all__ = [
     "DETFOLD_STAGED_REVERSE_DELIVERY", "DETFOLD_STAGED_SEPARATE_SCALE",
     "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
     "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
-    "detfold_loopback_allreduce_staged", "detfold_shard_plan",
-    "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
+    "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_noalloc",
+    "detfold_shard_plan", "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
     "STATUS",
 ]
 
@@ -39,8 +39,9 @@ DETFOLD_STAGED_SEPARATE_SCALE = 2
 STATUS = {
     "DETFOLD_OK": 0, "DETFOLD_ERR_NULL": -1, "DETFOLD_ERR_WORLD": -2, "DETFOLD_ERR_LEN": -3,
     "DETFOLD_ERR_ALIGN": -4, "DETFOLD_ERR_OVERLAP": -5, "DETFOLD_ERR_WORKSPACE": -6,
-    "DETFOLD_ERR_CUDA": -7, "DETFOLD_ERR_ARG": -8,
+    "DETFOLD_ERR_CUDA": -7, "DETFOLD_ERR_ARG": -8, "DETFOLD_ERR_SCRATCH_LIMIT": -9,
 }
+DETFOLD_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -61,6 +62,7 @@ lib.detfold_loopback_allreduce.argtypes = [_P, _INT, _I64, _F, _P]
 lib.detfold_staged_workspace_bytes.argtypes = [_I64, _INT]
 lib.detfold_staged_workspace_bytes.restype = _I64
 lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _INT, _P, _I64, _P]
+lib.detfold_loopback_allreduce_staged_noalloc.argtypes = [_P, _INT, _I64, _F, _INT, _P]
 lib.detfold_shard_plan.argtypes = [_I64, _INT, _P, _P]
 lib.detfold_status_string.argtypes = [_INT]
 lib.detfold_status_string.restype = ctypes.c_char_p
@@ -68,7 +70,7 @@ lib.detfold_last_cuda_error.argtypes = []
 lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
 for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
-              "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
+              "detfold_loopback_allreduce_staged_noalloc", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
     getattr(lib, _name).restype = _INT
 
 
@@ -156,6 +158,13 @@ def status_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: fl
                                                  workspace_bytes, _stream(stream))
 
 
+def status_loopback_allreduce_staged_noalloc(arenas, W: int, length: int, mean_scale: float,
+                                             flags: int, stream=None) -> int:
+    tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
+    return lib.detfold_loopback_allreduce_staged_noalloc(tab, W, length, mean_scale, flags,
+                                                         _stream(stream))
+
+
 # ------------------------------------------------------------------ raising calls (C names)
 
 def detfold_sum_stacked(out, stacked, W: int, length: int, stream=None) -> None:
@@ -188,6 +197,19 @@ def detfold_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: f
     _check(status_loopback_allreduce_staged(arenas, W, length, mean_scale, flags, workspace,
                                             workspace_bytes, stream),
            "detfold_loopback_allreduce_staged")
+
+
+def detfold_loopback_allreduce_staged_noalloc(arenas, W: int, length: int,
+                                              mean_scale: float = 1.0, flags: int = 0,
+                                              stream=None) -> None:
+    """The staged all-reduce with its scratch inside the library (no device
+    allocation by anyone): for callers that cannot allocate, such as code
+    running during CUDA-graph capture or under a fixed device-memory budget.
+    Requests larger than DETFOLD_NOALLOC_SCRATCH_BYTES of workspace raise
+    DETFOLD_ERR_SCRATCH_LIMIT; concurrent calls on unordered streams race on
+    the shared scratch."""
+    _check(status_loopback_allreduce_staged_noalloc(arenas, W, length, mean_scale, flags, stream),
+           "detfold_loopback_allreduce_staged_noalloc")
 
 
 def detfold_shard_plan(length: int, W: int) -> tuple[list[int], list[int]]:

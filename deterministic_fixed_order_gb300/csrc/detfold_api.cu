@@ -88,6 +88,10 @@ __global__ void empty_kernel(int pdl)
 
 namespace detfold {
 
+// Records a failed CUDA call for detfold_last_cuda_error (for entry points
+// defined in other translation units).
+int record_cuda_status(cudaError_t e) { return cuda_status(e); }
+
 cudaError_t launch_empty(int count, int pdl, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
@@ -270,6 +274,8 @@ const char *detfold_status_string(int status)
     case DETFOLD_ERR_WORKSPACE: return "workspace missing, too small or not 16-byte aligned";
     case DETFOLD_ERR_CUDA: return "a CUDA call failed (see detfold_last_cuda_error)";
     case DETFOLD_ERR_ARG: return "invalid argument";
+    case DETFOLD_ERR_SCRATCH_LIMIT:
+        return "request needs more than the library's static scratch (DETFOLD_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
     }
 }

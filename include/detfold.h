@@ -58,6 +58,7 @@ extern "C" {
 #define DETFOLD_ERR_WORKSPACE (-6) /* workspace missing, too small or misaligned     */
 #define DETFOLD_ERR_CUDA (-7)      /* a CUDA call failed; see detfold_last_cuda_error */
 #define DETFOLD_ERR_ARG (-8)       /* another invalid argument (unknown flag bits)   */
+#define DETFOLD_ERR_SCRATCH_LIMIT (-9) /* request needs more than the static scratch  */
 
 /* Flags of detfold_loopback_allreduce_staged. */
 #define DETFOLD_STAGED_REVERSE_DELIVERY 1 /* copy peers into the stack in descending rank order */
@@ -148,6 +149,33 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
  * Host only; touches no device.
  */
 int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens);
+
+/*
+ * Allocation-free staged loopback all-reduce. The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- code
+ * that runs while a stream is being captured into a CUDA graph (allocation
+ * is not permitted there), and runtimes whose device memory is owned and
+ * budgeted by their own allocator or reserved up front, where a stray
+ * allocation would fail or break the budget. It computes exactly what
+ * detfold_loopback_allreduce_staged computes, with the same arguments except
+ * the workspace: its scratch is a file-scope device array of
+ * DETFOLD_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - Requests whose workspace (detfold_staged_workspace_bytes(len, W)) is
+ *     larger than DETFOLD_NOALLOC_SCRATCH_BYTES return
+ *     DETFOLD_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array. Calls that overlap on the GPU (on
+ *     different streams without ordering between them) race on it; calls
+ *     ordered on one stream are safe. Nothing in the array needs to start
+ *     at zero: each call writes the stack rows before it reads them.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define DETFOLD_NOALLOC_SCRATCH_BYTES ((int64_t)16 << 20)
+int detfold_loopback_allreduce_staged_noalloc(float *const *arenas, int W, int64_t len,
+                                              float mean_scale, int flags, void *stream);
 
 /* A static, human-readable name for a status code. */
 const char *detfold_status_string(int status);

@@ -15,7 +15,7 @@ One step = one pass over every row of the hot path at its workload size:
 inputs resident in HBM. Algorithmic bytes per call: (W+1)*len*4 for a sum,
 2*len*4 for the mean pass, 2*W*len*4 for an all-reduce (the staged
 comparator is charged the same algorithmic bytes although it moves
-(5W-1)*len*4). The step reads and writes ~11 GB, far more than the 129 MB
+(4W+1)*len*4: exchange 2W, fold W+1, distribute W). The step reads and writes ~11 GB, far more than the 129 MB
 L2, so no L2 flush is needed between steps.
 
 Also reported: per-row kernel times from CUDA events on the launching
@@ -227,7 +227,7 @@ class Workload:
             ("c3_ptrs", lambda: df.detfold_sum_ptrs(self.c3_out2, self.c3_rows, C3_W, C3_N), 1),
             ("c4_fused", lambda: df.detfold_loopback_allreduce(self.c4f, C4_W, C4_N, self.scale4), 1),
             ("c4_staged", lambda: df.detfold_loopback_allreduce_staged(
-                self.c4s, C4_W, C4_N, self.scale4, 0, self.ws, self.ws_bytes), C4_W),
+                self.c4s, C4_W, C4_N, self.scale4, 0, self.ws, self.ws_bytes), 3 * C4_W),
         ]
         for W in C5_WS:
             def c5(W=W):
@@ -481,10 +481,10 @@ def run_gpu(args) -> None:
     c3_ms = (per_row["c3_stacked"]["ms"] + per_row["c3_ptrs"]["ms"]) / 2
     c4_ms = per_row["c4_fused"]["ms"]
     if 2 * c3_ms >= c4_ms:
-        dom, dom_bytes, dom_ms = ("fold_vec_kernel<W=8,VEC=4,kSumNC> (c3_stacked+c3_ptrs)",
+        dom, dom_bytes, dom_ms = ("fold_vec_kernel<W=8,kSumNC> (c3_stacked+c3_ptrs)",
                                   bytes_by_row["c3_stacked"], c3_ms)
     else:
-        dom, dom_bytes, dom_ms = ("fold_vec_kernel<W=4,VEC=4,kAllReduce> (c4_fused)",
+        dom, dom_bytes, dom_ms = ("fold_vec_kernel<W=4,kAllReduce> (c4_fused)",
                                   bytes_by_row["c4_fused"], c4_ms)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     khash = kernel_source_hash()

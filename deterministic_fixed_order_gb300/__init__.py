@@ -21,7 +21,8 @@ from . import build as _build
 
 __all__ = [
     "DetfoldError", "lib", "DETFOLD_MAX_W", "DETFOLD_MAX_LEN",
-    "DETFOLD_STAGED_REVERSE_DELIVERY", "DETFOLD_STAGED_SEPARATE_SCALE",
+    "DETFOLD_STAGED_REVERSE_DELIVERY", "DETFOLD_STAGED_SEPARATE_SCALE", "DETFOLD_STAGED_CE_COPIES",
+    "detfold_broadcast", "detfold_all_gather",
     "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
     "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
     "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_noalloc",
@@ -35,6 +36,7 @@ DETFOLD_MAX_W = 256
 DETFOLD_MAX_LEN = 1 << 40
 DETFOLD_STAGED_REVERSE_DELIVERY = 1
 DETFOLD_STAGED_SEPARATE_SCALE = 2
+DETFOLD_STAGED_CE_COPIES = 4
 
 STATUS = {
     "DETFOLD_OK": 0, "DETFOLD_ERR_NULL": -1, "DETFOLD_ERR_WORLD": -2, "DETFOLD_ERR_LEN": -3,
@@ -63,6 +65,8 @@ lib.detfold_staged_workspace_bytes.argtypes = [_I64, _INT]
 lib.detfold_staged_workspace_bytes.restype = _I64
 lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _INT, _P, _I64, _P]
 lib.detfold_loopback_allreduce_staged_noalloc.argtypes = [_P, _INT, _I64, _F, _INT, _P]
+lib.detfold_broadcast.argtypes = [_P, _INT, _P, _I64, _P]
+lib.detfold_all_gather.argtypes = [_P, _INT, _P, _I64, _P]
 lib.detfold_shard_plan.argtypes = [_I64, _INT, _P, _P]
 lib.detfold_status_string.argtypes = [_INT]
 lib.detfold_status_string.restype = ctypes.c_char_p
@@ -70,7 +74,8 @@ lib.detfold_last_cuda_error.argtypes = []
 lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
 for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
-              "detfold_loopback_allreduce_staged_noalloc", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
+              "detfold_loopback_allreduce_staged_noalloc", "detfold_broadcast",
+              "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
     getattr(lib, _name).restype = _INT
 
 
@@ -165,6 +170,17 @@ def status_loopback_allreduce_staged_noalloc(arenas, W: int, length: int, mean_s
                                                          _stream(stream))
 
 
+def status_broadcast(dsts, ndst: int, src, length: int, stream=None) -> int:
+    tab = _ptr_array(dsts, length, "dsts") if dsts is not None else None
+    return lib.detfold_broadcast(tab, ndst, _dev_ptr(src, length, "src"), length, _stream(stream))
+
+
+def status_all_gather(outs, W: int, parts, span: int, stream=None) -> int:
+    otab = _ptr_array(outs, W * span, "outs") if outs is not None else None
+    ptab = _ptr_array(parts, span, "parts") if parts is not None else None
+    return lib.detfold_all_gather(otab, W, ptab, span, _stream(stream))
+
+
 # ------------------------------------------------------------------ raising calls (C names)
 
 def detfold_sum_stacked(out, stacked, W: int, length: int, stream=None) -> None:
@@ -210,6 +226,14 @@ def detfold_loopback_allreduce_staged_noalloc(arenas, W: int, length: int,
     the shared scratch."""
     _check(status_loopback_allreduce_staged_noalloc(arenas, W, length, mean_scale, flags, stream),
            "detfold_loopback_allreduce_staged_noalloc")
+
+
+def detfold_broadcast(dsts, ndst: int, src, length: int, stream=None) -> None:
+    _check(status_broadcast(dsts, ndst, src, length, stream), "detfold_broadcast")
+
+
+def detfold_all_gather(outs, W: int, parts, span: int, stream=None) -> None:
+    _check(status_all_gather(outs, W, parts, span, stream), "detfold_all_gather")
 
 
 def detfold_shard_plan(length: int, W: int) -> tuple[list[int], list[int]]:

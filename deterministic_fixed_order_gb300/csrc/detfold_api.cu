@@ -1,6 +1,6 @@
 // The C ABI of libdetfold (declared in include/detfold.h): argument
-// validation, the shard plan, dispatch to the fold launchers, and the staged
-// comparator's copy schedule. Nothing here allocates, synchronizes or
+// validation, the shard plan, dispatch to the fold and movement launchers,
+// and the staged comparator's schedule. Nothing here allocates, synchronizes or
 // touches device memory other than through stream-ordered launches and
 // copies.
 #include <cstdint>
@@ -195,7 +195,8 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len, 
     if (!arenas) return DETFOLD_ERR_NULL;
     if (int rc = check_world(W)) return rc;
     if (int rc = check_len(len)) return rc;
-    if (flags & ~(DETFOLD_STAGED_REVERSE_DELIVERY | DETFOLD_STAGED_SEPARATE_SCALE))
+    if (flags & ~(DETFOLD_STAGED_REVERSE_DELIVERY | DETFOLD_STAGED_SEPARATE_SCALE |
+                  DETFOLD_STAGED_CE_COPIES))
         return DETFOLD_ERR_ARG;
     if (int rc = arenas_valid(arenas, W, len)) return rc;
     const bool do_scale = mean_scale != 1.0f;
@@ -218,6 +219,8 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len, 
     const bool reverse = flags & DETFOLD_STAGED_REVERSE_DELIVERY;
     const bool separate = flags & DETFOLD_STAGED_SEPARATE_SCALE;
 
+    const bool ce = flags & DETFOLD_STAGED_CE_COPIES;
+
     // Phase A: per owner, exchange into slot = source rank, then fold.
     for (int o = 0; o < W; ++o) {
         const int64_t n = lens[o], s0 = starts[o];
@@ -226,11 +229,21 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len, 
         const int ph = detfold::elem_phase(dst, 8);  // rows share the shard's 32-byte phase
         const float *rows[DETFOLD_MAX_W];
         for (int r = 0; r < W; ++r) rows[r] = ws + (int64_t)r * stride + ph;
+        const float *from[DETFOLD_MAX_W];
+        float *to[DETFOLD_MAX_W];
         for (int k = 0; k < W; ++k) {
             const int src = reverse ? W - 1 - k : k;
-            cudaError_t e = cudaMemcpyAsync((void *)rows[src], arenas[src] + s0, (size_t)n * 4,
-                                            cudaMemcpyDeviceToDevice, st);
-            if (e != cudaSuccess) return cuda_status(e);
+            from[k] = arenas[src] + s0;
+            to[k] = const_cast<float *>(rows[src]);
+        }
+        if (ce) {
+            for (int k = 0; k < W; ++k) {
+                cudaError_t e = cudaMemcpyAsync(to[k], from[k], (size_t)n * 4,
+                                                cudaMemcpyDeviceToDevice, st);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
+        } else if (int rc = cuda_status(detfold::launch_move(from, to, W, n, st))) {
+            return rc;
         }
         detfold::LaunchSpec s = {W, detfold::kSumNC, rows, dst, n, mean_scale,
                                  (do_scale && !separate) ? 1 : 0};
@@ -243,12 +256,71 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len, 
     for (int o = 0; o < W; ++o) {
         const int64_t n = lens[o], s0 = starts[o];
         if (n == 0) continue;
+        const float *from[DETFOLD_MAX_W];
+        float *to[DETFOLD_MAX_W];
+        int K = 0;
         for (int r = 0; r < W; ++r) {
             if (r == o) continue;
-            cudaError_t e = cudaMemcpyAsync(arenas[r] + s0, arenas[o] + s0, (size_t)n * 4,
-                                            cudaMemcpyDeviceToDevice, st);
-            if (e != cudaSuccess) return cuda_status(e);
+            from[K] = arenas[o] + s0;
+            to[K++] = arenas[r] + s0;
         }
+        if (ce) {
+            for (int k = 0; k < K; ++k) {
+                cudaError_t e = cudaMemcpyAsync(to[k], from[k], (size_t)n * 4,
+                                                cudaMemcpyDeviceToDevice, st);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
+        } else if (int rc = cuda_status(detfold::launch_move(from, to, K, n, st))) {
+            return rc;
+        }
+    }
+    return DETFOLD_OK;
+}
+
+int detfold_broadcast(float *const *dsts, int ndst, const float *src, int64_t len, void *stream)
+{
+    if (!dsts || !src) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(ndst)) return rc;
+    for (int k = 0; k < ndst; ++k)
+        if (!dsts[k]) return DETFOLD_ERR_NULL;
+    if (int rc = check_len(len)) return rc;
+    if (!aligned4(src)) return DETFOLD_ERR_ALIGN;
+    if (int rc = arenas_valid(dsts, ndst, len)) return rc;
+    if (len == 0) return DETFOLD_OK;
+    for (int k = 0; k < ndst; ++k)
+        if (intersects(dsts[k], len * 4, src, len * 4)) return DETFOLD_ERR_OVERLAP;
+    const float *from[DETFOLD_MAX_W];
+    for (int k = 0; k < ndst; ++k) from[k] = src;
+    return cuda_status(detfold::launch_move(from, dsts, ndst, len, (cudaStream_t)stream));
+}
+
+int detfold_all_gather(float *const *outs, int W, const float *const *parts, int64_t span,
+                       void *stream)
+{
+    if (!outs || !parts) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    for (int r = 0; r < W; ++r)
+        if (!outs[r] || !parts[r]) return DETFOLD_ERR_NULL;
+    if (int rc = check_len(span)) return rc;
+    if ((int64_t)W * span > DETFOLD_MAX_LEN) return DETFOLD_ERR_LEN;
+    for (int r = 0; r < W; ++r)
+        if (!aligned4(parts[r])) return DETFOLD_ERR_ALIGN;
+    const int64_t total = (int64_t)W * span;
+    if (int rc = arenas_valid(outs, W, total)) return rc;
+    if (span == 0) return DETFOLD_OK;
+    for (int r = 0; r < W; ++r)
+        for (int p = 0; p < W; ++p)
+            if (intersects(outs[r], total * 4, parts[p], span * 4)) return DETFOLD_ERR_OVERLAP;
+    // Part p lands at offset p*span of every output: one broadcast per part.
+    for (int p = 0; p < W; ++p) {
+        const float *from[DETFOLD_MAX_W];
+        float *to[DETFOLD_MAX_W];
+        for (int r = 0; r < W; ++r) {
+            from[r] = parts[p];
+            to[r] = outs[r] + (int64_t)p * span;
+        }
+        if (int rc = cuda_status(detfold::launch_move(from, to, W, span, (cudaStream_t)stream)))
+            return rc;
     }
     return DETFOLD_OK;
 }

@@ -33,9 +33,90 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+// Launch-shape knobs (compile-time; the defaults are the measured choice).
+#ifndef DETFOLD_PREFER_VEC
+#define DETFOLD_PREFER_VEC 8  // 8 = 32-byte vectors, 4 = 16-byte vectors
+#endif
+#ifndef DETFOLD_SUM_INFLIGHT
+#define DETFOLD_SUM_INFLIGHT 256  // loaded bytes per thread per unrolled group, sum modes
+#endif
+#ifndef DETFOLD_AR_INFLIGHT
+#define DETFOLD_AR_INFLIGHT 256  // the same for the all-reduce mode
+#endif
+#ifndef DETFOLD_SUM_MAX_FLOATS
+#define DETFOLD_SUM_MAX_FLOATS 32  // cap on loaded floats per thread per group (U > 1), sum modes
+#endif
+#ifndef DETFOLD_SCALAR_INFLIGHT
+#define DETFOLD_SCALAR_INFLIGHT 32  // the same for the scalar (mismatched-phase) kernels
+#endif
+#ifndef DETFOLD_SCALAR_MAX_U
+#define DETFOLD_SCALAR_MAX_U 16
+#endif
+#ifndef DETFOLD_SMALL_LEN
+#define DETFOLD_SMALL_LEN (1 << 17)  // elements at or below: small-payload launch
+#endif
+#ifndef DETFOLD_SMALL_THREADS
+#define DETFOLD_SMALL_THREADS 128
+#endif
+#ifndef DETFOLD_SUM_THREADS
+#define DETFOLD_SUM_THREADS 1024  // CTA size of the bandwidth path, sum modes
+#endif
+#ifndef DETFOLD_AR_THREADS
+#define DETFOLD_AR_THREADS 256  // CTA size of the bandwidth path, all-reduce mode
+#endif
+#ifndef DETFOLD_SMALL_PDL
+#define DETFOLD_SMALL_PDL 1  // programmatic dependent launch on the small path
+#endif
+#ifndef DETFOLD_SUM_CTAS_PER_SM
+#define DETFOLD_SUM_CTAS_PER_SM 1  // 0: as many as fit; else at most this many per SM
+#endif
+#ifndef DETFOLD_AR_CTAS_PER_SM
+#define DETFOLD_AR_CTAS_PER_SM 0
+#endif
+
+// Cache-hint knobs (compile-time; the defaults are the measured choice).
+#ifndef DETFOLD_LD_L2_PREFETCH
+#define DETFOLD_LD_L2_PREFETCH 0  // 0, 128 or 256: L2 prefetch size hint on vector loads
+#endif
+#ifndef DETFOLD_ST_HINT
+#define DETFOLD_ST_HINT 0  // 0: default write-back, 1: .cs (streaming), 2: .L1::no_allocate
+#endif
+#if DETFOLD_LD_L2_PREFETCH == 256
+#define DETFOLD_LD_PF ".L2::256B"
+#elif DETFOLD_LD_L2_PREFETCH == 128
+#define DETFOLD_LD_PF ".L2::128B"
+#else
+#define DETFOLD_LD_PF ""
+#endif
+#if DETFOLD_ST_HINT == 1
+#define DETFOLD_ST_Q ".cs"
+#elif DETFOLD_ST_HINT == 2
+#define DETFOLD_ST_Q ".L1::no_allocate"
+#else
+#define DETFOLD_ST_Q ""
+#endif
+
 namespace detfold {
 
 enum Mode : int { kSumNC = 0, kSumCoherent = 1, kAllReduce = 2 };
+
+// CTA size of the bandwidth path, and the launch bound that also admits the
+// small path's CTAs.
+template <int MODE>
+constexpr int bw_threads()
+{
+    return MODE == kAllReduce ? DETFOLD_AR_THREADS : DETFOLD_SUM_THREADS;
+}
+template <int MODE>
+constexpr int ctas_per_sm_cap()
+{
+    return MODE == kAllReduce ? DETFOLD_AR_CTAS_PER_SM : DETFOLD_SUM_CTAS_PER_SM;
+}
+template <int MODE>
+constexpr int max_threads()
+{
+    return bw_threads<MODE>() > DETFOLD_SMALL_THREADS ? bw_threads<MODE>() : DETFOLD_SMALL_THREADS;
+}
 
 constexpr int kGenericW = 256;  // table capacity of the runtime-W kernels
 
@@ -52,6 +133,17 @@ struct FoldParams {
     int pdl;               // launched with programmatic dependent launch
 };
 
+// Pure-movement launches: K (source -> destination) pairs of equal length.
+// 250 pairs keep the parameter block under 4 KB; longer lists are split.
+constexpr int kMaxPairs = 250;
+struct MoveParams {
+    const float *src[kMaxPairs];
+    float *dst[kMaxPairs];
+    int64_t len, head, nvec;
+    int K;
+    int pdl;
+};
+
 template <int VEC>
 struct alignas(VEC * 4) Vec {
     float v[VEC];
@@ -66,7 +158,7 @@ __device__ __forceinline__ float ld1(const float *p)
     if constexpr (NC)
         asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(x) : "l"(p));
     else
-        asm volatile("ld.global.L1::no_allocate.f32 %0, [%1];" : "=f"(x) : "l"(p) : "memory");
+        asm volatile("ld.global.L1::no_allocate.f32 %0, [%1];" : "=f"(x) : "l"(p));
     return x;
 }
 
@@ -76,27 +168,25 @@ __device__ __forceinline__ Vec<VEC> ldv(const float *p)
     Vec<VEC> r;
     if constexpr (VEC == 4) {
         if constexpr (NC)
-            asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+            asm volatile("ld.global.nc.L1::no_allocate" DETFOLD_LD_PF ".v4.f32 {%0,%1,%2,%3}, [%4];"
                 : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3])
                 : "l"(p));
         else
-            asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+            asm volatile("ld.global.L1::no_allocate" DETFOLD_LD_PF ".v4.f32 {%0,%1,%2,%3}, [%4];"
                          : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3])
-                         : "l"(p)
-                         : "memory");
+                         : "l"(p));
     } else {
         static_assert(VEC == 8, "VEC is 4 or 8");
         if constexpr (NC)
-            asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            asm volatile("ld.global.nc.L1::no_allocate" DETFOLD_LD_PF ".v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                 : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
                   "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
                 : "l"(p));
         else
-            asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            asm volatile("ld.global.L1::no_allocate" DETFOLD_LD_PF ".v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                          : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]),
                            "=f"(r.v[4]), "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
-                         : "l"(p)
-                         : "memory");
+                         : "l"(p));
     }
     return r;
 }
@@ -110,11 +200,11 @@ template <int VEC>
 __device__ __forceinline__ void stv(float *p, const Vec<VEC> &x)
 {
     if constexpr (VEC == 4)
-        asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(x.v[0]), "f"(x.v[1]),
+        asm volatile("st.global" DETFOLD_ST_Q ".v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(x.v[0]), "f"(x.v[1]),
                      "f"(x.v[2]), "f"(x.v[3])
                      : "memory");
     else
-        asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(x.v[0]),
+        asm volatile("st.global" DETFOLD_ST_Q ".v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(x.v[0]),
                      "f"(x.v[1]), "f"(x.v[2]), "f"(x.v[3]), "f"(x.v[4]), "f"(x.v[5]),
                      "f"(x.v[6]), "f"(x.v[7])
                      : "memory");
@@ -176,7 +266,7 @@ __device__ __forceinline__ void store_result(const FoldParams<NT> &p, int64_t e,
 // U vectors per thread per iteration, grid-stride; every operand shares the
 // same VEC*4-byte phase. Element index of vector v is head + v*VEC.
 template <int W, int VEC, int U, int MODE>
-__global__ void __launch_bounds__(256) fold_vec_kernel(const __grid_constant__ FoldParams<W> p)
+__global__ void __launch_bounds__(max_threads<MODE>()) fold_vec_kernel(const __grid_constant__ FoldParams<W> p)
 {
     constexpr bool NC = (MODE == kSumNC);
     pdl_enter(p.pdl);
@@ -222,7 +312,7 @@ __global__ void __launch_bounds__(256) fold_vec_kernel(const __grid_constant__ F
 // Operands at different 4-byte phases: coalesced scalar accesses, U elements
 // per thread per iteration with all U*W loads issued first.
 template <int W, int U, int MODE>
-__global__ void __launch_bounds__(256) fold_scalar_kernel(const __grid_constant__ FoldParams<W> p)
+__global__ void __launch_bounds__(max_threads<MODE>()) fold_scalar_kernel(const __grid_constant__ FoldParams<W> p)
 {
     constexpr bool NC = (MODE == kSumNC);
     pdl_enter(p.pdl);
@@ -253,25 +343,26 @@ __global__ void __launch_bounds__(256) fold_scalar_kernel(const __grid_constant_
 
 // ---------------------------------------------------------------- runtime-W kernels (W > 8)
 
-// Loads are issued eight ranks at a time ahead of their adds; the chain
-// order is unchanged.
+// Loads are issued G ranks at a time ahead of their adds (G*VEC*4 = 128
+// bytes per thread); the chain order is unchanged.
 template <int VEC, int MODE>
-__global__ void __launch_bounds__(256) fold_vec_generic_kernel(const __grid_constant__ FoldParams<kGenericW> p)
+__global__ void __launch_bounds__(max_threads<MODE>()) fold_vec_generic_kernel(const __grid_constant__ FoldParams<kGenericW> p)
 {
     constexpr bool NC = (MODE == kSumNC);
+    constexpr int G = 32 / VEC;
     pdl_enter(p.pdl);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (int64_t v = gtid; v < p.nvec; v += stride) {
         const int64_t e = p.head + v * VEC;
         Vec<VEC> acc = ldv<VEC, NC>(p.src[0] + e);
-        for (int r0 = 1; r0 < p.W; r0 += 8) {
-            Vec<VEC> x[8];
+        for (int r0 = 1; r0 < p.W; r0 += G) {
+            Vec<VEC> x[G];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < G; ++k)
                 if (r0 + k < p.W) x[k] = ldv<VEC, NC>(p.src[r0 + k] + e);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < G; ++k)
                 if (r0 + k < p.W)
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) acc.v[j] = __fadd_rn(acc.v[j], x[k].v[j]);
@@ -284,7 +375,7 @@ __global__ void __launch_bounds__(256) fold_vec_generic_kernel(const __grid_cons
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(256) fold_scalar_generic_kernel(const __grid_constant__ FoldParams<kGenericW> p)
+__global__ void __launch_bounds__(max_threads<MODE>()) fold_scalar_generic_kernel(const __grid_constant__ FoldParams<kGenericW> p)
 {
     constexpr bool NC = (MODE == kSumNC);
     pdl_enter(p.pdl);

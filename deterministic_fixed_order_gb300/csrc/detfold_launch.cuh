@@ -9,22 +9,6 @@
 
 #include "detfold_kernels.cuh"
 
-#ifndef DETFOLD_PREFER_VEC
-#define DETFOLD_PREFER_VEC 4  // 4 = 16-byte vectors, 8 = 32-byte vectors
-#endif
-#ifndef DETFOLD_INFLIGHT_BYTES
-#define DETFOLD_INFLIGHT_BYTES 128  // loaded bytes per thread per unrolled group
-#endif
-#ifndef DETFOLD_SMALL_LEN
-#define DETFOLD_SMALL_LEN (1 << 17)  // elements at or below: small-payload launch
-#endif
-#ifndef DETFOLD_SMALL_THREADS
-#define DETFOLD_SMALL_THREADS 128
-#endif
-#ifndef DETFOLD_BW_THREADS
-#define DETFOLD_BW_THREADS 256
-#endif
-
 namespace detfold {
 
 // One fold launch as the API layer describes it.
@@ -67,18 +51,24 @@ inline Plan make_plan(const LaunchSpec &s)
     return Plan{0, 0, 0};
 }
 
+// Vectors (or scalars, vec == 0) per thread per unrolled group.
+template <int MODE>
 inline constexpr int u_for(int W, int vec)
 {
-    // vec == 0: scalar kernel, 4-byte loads
-    return (DETFOLD_INFLIGHT_BYTES / ((vec ? vec : 1) * 4 * W)) > 0
-               ? (DETFOLD_INFLIGHT_BYTES / ((vec ? vec : 1) * 4 * W))
-               : 1;
+    if (vec == 0) {
+        const int u = DETFOLD_SCALAR_INFLIGHT / (4 * W);
+        return u < 1 ? 1 : (u > DETFOLD_SCALAR_MAX_U ? DETFOLD_SCALAR_MAX_U : u);
+    }
+    const int bytes = MODE == kAllReduce ? DETFOLD_AR_INFLIGHT : DETFOLD_SUM_INFLIGHT;
+    int u = bytes / (vec * 4 * W);
+    if (MODE != kAllReduce && u * W * vec > DETFOLD_SUM_MAX_FLOATS) u = DETFOLD_SUM_MAX_FLOATS / (W * vec);
+    return u < 1 ? 1 : u;
 }
 
 // Resident CTAs the whole GPU holds for `kernel` at `threads` per CTA,
 // computed once per (instantiation, device).
 template <typename Kernel>
-inline cudaError_t resident_ctas(Kernel kernel, int threads, int *out)
+inline cudaError_t resident_ctas(Kernel kernel, int threads, int cap_per_sm, int *out)
 {
     static std::atomic<int> cache[64];
     int dev = 0;
@@ -92,6 +82,7 @@ inline cudaError_t resident_ctas(Kernel kernel, int threads, int *out)
         if (e != cudaSuccess) return e;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
         if (e != cudaSuccess) return e;
+        if (cap_per_sm > 0 && per_sm > cap_per_sm) per_sm = cap_per_sm;
         v = sms * (per_sm > 0 ? per_sm : 1);
         cache[dev].store(v, std::memory_order_relaxed);
     }
@@ -101,15 +92,15 @@ inline cudaError_t resident_ctas(Kernel kernel, int threads, int *out)
 
 template <typename Params>
 inline cudaError_t launch_kernel(void (*kernel)(Params), const Params &p, int64_t work, int u,
-                                 bool small, cudaStream_t stream)
+                                 bool small, int bw_threads, int cap_per_sm, cudaStream_t stream)
 {
-    const int threads = small ? DETFOLD_SMALL_THREADS : DETFOLD_BW_THREADS;
+    const int threads = small ? DETFOLD_SMALL_THREADS : bw_threads;
     int64_t blocks = (work + threads - 1) / threads;
     if (!small) {
         const int64_t per_iter = (int64_t)threads * u;
         blocks = (work + per_iter - 1) / per_iter;
         int cap = 0;
-        const cudaError_t e = resident_ctas(kernel, threads, &cap);
+        const cudaError_t e = resident_ctas(kernel, threads, cap_per_sm, &cap);
         if (e != cudaSuccess) return e;
         if (blocks > cap) blocks = cap;
     }
@@ -121,7 +112,7 @@ inline cudaError_t launch_kernel(void (*kernel)(Params), const Params &p, int64_
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    if (small) {
+    if (small && DETFOLD_SMALL_PDL) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -142,7 +133,7 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
     p.scale = s.scale;
     p.do_scale = s.do_scale;
     p.W = s.W;
-    p.pdl = small ? 1 : 0;
+    p.pdl = (small && DETFOLD_SMALL_PDL) ? 1 : 0;
     return p;
 }
 
@@ -152,16 +143,18 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
     const Plan pl = make_plan(s);
     const bool small = s.len <= DETFOLD_SMALL_LEN;
     const FoldParams<W> p = fill_params<W>(s, pl, small);
+    constexpr int T = bw_threads<MODE>();
+    constexpr int C = ctas_per_sm_cap<MODE>();
     if (pl.vec == 8) {
-        constexpr int U = u_for(W, 8);
-        return launch_kernel(fold_vec_kernel<W, 8, U, MODE>, p, pl.nvec, U, small, stream);
+        constexpr int U = u_for<MODE>(W, 8);
+        return launch_kernel(fold_vec_kernel<W, 8, U, MODE>, p, pl.nvec, U, small, T, C, stream);
     }
     if (pl.vec == 4) {
-        constexpr int U = u_for(W, 4);
-        return launch_kernel(fold_vec_kernel<W, 4, U, MODE>, p, pl.nvec, U, small, stream);
+        constexpr int U = u_for<MODE>(W, 4);
+        return launch_kernel(fold_vec_kernel<W, 4, U, MODE>, p, pl.nvec, U, small, T, C, stream);
     }
-    constexpr int U = u_for(W, 0);
-    return launch_kernel(fold_scalar_kernel<W, U, MODE>, p, s.len, U, small, stream);
+    constexpr int U = u_for<MODE>(W, 0);
+    return launch_kernel(fold_scalar_kernel<W, U, MODE>, p, s.len, U, small, T, C, stream);
 }
 
 template <int MODE>
@@ -170,9 +163,11 @@ inline cudaError_t launch_generic(const LaunchSpec &s, cudaStream_t stream)
     const Plan pl = make_plan(s);
     const bool small = s.len <= DETFOLD_SMALL_LEN;
     const FoldParams<kGenericW> p = fill_params<kGenericW>(s, pl, small);
-    if (pl.vec == 8) return launch_kernel(fold_vec_generic_kernel<8, MODE>, p, pl.nvec, 1, small, stream);
-    if (pl.vec == 4) return launch_kernel(fold_vec_generic_kernel<4, MODE>, p, pl.nvec, 1, small, stream);
-    return launch_kernel(fold_scalar_generic_kernel<MODE>, p, s.len, 1, small, stream);
+    constexpr int T = bw_threads<MODE>();
+    constexpr int C = ctas_per_sm_cap<MODE>();
+    if (pl.vec == 8) return launch_kernel(fold_vec_generic_kernel<8, MODE>, p, pl.nvec, 1, small, T, C, stream);
+    if (pl.vec == 4) return launch_kernel(fold_vec_generic_kernel<4, MODE>, p, pl.nvec, 1, small, T, C, stream);
+    return launch_kernel(fold_scalar_generic_kernel<MODE>, p, s.len, 1, small, T, C, stream);
 }
 
 template <int MODE>
@@ -197,5 +192,8 @@ cudaError_t launch_sum_nc(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_sum_coherent(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_allreduce(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_empty(int count, int pdl, cudaStream_t stream);
+// Pure movement of K pairs (move_kernels.cu); K may exceed kMaxPairs.
+cudaError_t launch_move(const float *const *src, float *const *dst, int K, int64_t len,
+                        cudaStream_t stream);
 
 }  // namespace detfold

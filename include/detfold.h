@@ -63,6 +63,8 @@ extern "C" {
 /* Flags of detfold_loopback_allreduce_staged. */
 #define DETFOLD_STAGED_REVERSE_DELIVERY 1 /* copy peers into the stack in descending rank order */
 #define DETFOLD_STAGED_SEPARATE_SCALE 2   /* mean multiply as its own pass, not in the fold store */
+#define DETFOLD_STAGED_CE_COPIES 4        /* move bytes with cudaMemcpyAsync (copy engines), as the
+                                             reference's copy_d2d does, instead of the SM movement kernel */
 
 /*
  * Stacked fold (mamba-rs src/dist/reducer.rs, `DET_SUM_RANKS_SRC` and
@@ -123,12 +125,15 @@ int64_t detfold_staged_workspace_bytes(int64_t len, int W);
  * (mamba-rs src/dist/reducer.rs, `LoopbackWorld::run_round`), kept as the
  * comparator of the fused call. For each owner o with a non-empty shard
  * (detfold_shard_plan): copy every rank's slice of that shard into stack
- * slot = source rank (device-to-device copies, ascending rank order, or
- * descending with DETFOLD_STAGED_REVERSE_DELIVERY -- the bits must not
- * change), fold the slots into arena o's shard, and apply mean_scale in the
- * fold's store (or as a separate pass with DETFOLD_STAGED_SEPARATE_SCALE).
- * Then copy every owner's shard to all other arenas. Same end state and
- * bits as detfold_loopback_allreduce.
+ * slot = source rank (ascending rank order, or descending with
+ * DETFOLD_STAGED_REVERSE_DELIVERY -- the bits must not change), fold the
+ * slots into arena o's shard, and apply mean_scale in the fold's store (or
+ * as a separate pass with DETFOLD_STAGED_SEPARATE_SCALE). Then copy every
+ * owner's shard to all other arenas. The copies are pure byte movement: one
+ * SM movement launch per phase and owner by default (the distribute phase
+ * reads the owner's shard once for its W-1 destinations), or one
+ * cudaMemcpyAsync per copy with DETFOLD_STAGED_CE_COPIES. Same end state
+ * and bits as detfold_loopback_allreduce.
  *   arenas    host array of W device pointers (as above, pairwise disjoint).
  *   workspace device, >= detfold_staged_workspace_bytes(len, W) bytes,
  *             16-byte aligned, disjoint from every arena; contents on entry
@@ -139,6 +144,30 @@ int64_t detfold_staged_workspace_bytes(int64_t len, int W);
 int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
                                       float mean_scale, int flags, void *workspace,
                                       int64_t workspace_bytes, void *stream);
+
+/*
+ * Broadcast, pure byte movement (memra-engine 0.128.0 tests/tp_ar_gpu.rs,
+ * `broadcast_and_all_gather_move_bytes_exactly`: rank 0's buffer lands on
+ * every other rank byte for byte): dsts[k][i] = src[i] for every k.
+ *   dsts  host array of ndst device pointers, each to len f32, written;
+ *         pairwise disjoint and disjoint from src (DETFOLD_ERR_OVERLAP).
+ *   src   device, len f32, read.
+ * 1 <= ndst <= DETFOLD_MAX_W (DETFOLD_ERR_WORLD). One launch reads src once.
+ */
+int detfold_broadcast(float *const *dsts, int ndst, const float *src, int64_t len, void *stream);
+
+/*
+ * All-gather, pure byte movement (same test): every output receives the
+ * concatenation of the W parts in rank order,
+ *     outs[r][p * span + j] = parts[p][j]   for all r, p < W and j < span.
+ *   outs   host array of W device pointers, each to W * span f32, written;
+ *          pairwise disjoint and disjoint from every part.
+ *   parts  host array of W device pointers, each to span f32, read (parts
+ *          may overlap each other).
+ * One movement launch per part.
+ */
+int detfold_all_gather(float *const *outs, int W, const float *const *parts, int64_t span,
+                       void *stream);
 
 /*
  * Contiguous owner shards (imported as `shard_plan` by mamba-rs

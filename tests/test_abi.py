@@ -90,13 +90,27 @@ def test_workspace_bytes(df):
 
 
 # Fake device addresses: validation rejects these calls before any launch.
+# They are passed only where no GPU exists, so that a validation gap can
+# never turn into a launch on addresses that are not device memory.
 A = 1 << 32
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available() or os.path.exists("/dev/nvidia0")
+    except Exception:
+        return True  # unknown: assume a GPU
+
+
+no_gpu_only = pytest.mark.skipif(_has_gpu(), reason="fake device addresses only where no GPU exists")
 
 
 def _tab(*ptrs):
     return (ctypes.c_void_p * len(ptrs))(*ptrs)
 
 
+@no_gpu_only
 def test_validation_sum_stacked(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_sum_stacked(None, A, 2, 8, None) == S["DETFOLD_ERR_NULL"]
@@ -114,6 +128,7 @@ def test_validation_sum_stacked(df):
     assert L.detfold_sum_stacked(A, A, 2, 0, None) == S["DETFOLD_OK"]
 
 
+@no_gpu_only
 def test_validation_sum_ptrs(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_sum_ptrs(A, None, 2, 8, None) == S["DETFOLD_ERR_NULL"]
@@ -127,6 +142,7 @@ def test_validation_sum_ptrs(df):
     assert L.detfold_sum_ptrs(A, _tab(A), 1, 8, None) == S["DETFOLD_OK"]
 
 
+@no_gpu_only
 def test_validation_allreduce(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_loopback_allreduce(None, 2, 8, 1.0, None) == S["DETFOLD_ERR_NULL"]
@@ -140,12 +156,13 @@ def test_validation_allreduce(df):
     assert L.detfold_loopback_allreduce(_tab(A), 1, 8, 1.0, None) == S["DETFOLD_OK"]
 
 
+@no_gpu_only
 def test_validation_staged(df):
     L, S = df.lib, df.STATUS
     ws_need = df.detfold_staged_workspace_bytes(64, 2)
     arenas = _tab(A, A + 4096)
     W_ = A + (1 << 20)
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 4, W_, ws_need, None) == S["DETFOLD_ERR_ARG"]
+    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 8, W_, ws_need, None) == S["DETFOLD_ERR_ARG"]
     assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, None, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
     assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, W_, ws_need - 4, None) == S["DETFOLD_ERR_WORKSPACE"]
     assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, W_ + 8, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
@@ -154,6 +171,28 @@ def test_validation_staged(df):
     assert L.detfold_loopback_allreduce_staged(arenas, 2, 0, 0.5, 0, None, 0, None) == S["DETFOLD_OK"]
 
 
+@no_gpu_only
+def test_validation_broadcast_and_all_gather(df):
+    L, S = df.lib, df.STATUS
+    assert L.detfold_broadcast(None, 2, A, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_broadcast(_tab(A, A + 4096), 2, None, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_broadcast(_tab(A, A + 4096), 0, A + 8192, 8, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_broadcast(_tab(A, A + 4096), 2, A + 8194, 8, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_broadcast(_tab(A, A + 16), 2, A + 8192, 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_broadcast(_tab(A, A + 4096), 2, A + 4, 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_broadcast(_tab(A, A + 4096), 2, A + 8192, 0, None) == S["DETFOLD_OK"]
+    outs = _tab(A, A + 4096)
+    parts = _tab(A + 8192, A + 8192 + 64)
+    assert L.detfold_all_gather(None, 2, parts, 8, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_all_gather(outs, 0, parts, 8, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_all_gather(outs, 2, parts, -1, None) == S["DETFOLD_ERR_LEN"]
+    assert L.detfold_all_gather(_tab(A, A + 32), 2, parts, 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_all_gather(outs, 2, _tab(A + 8, A + 8192), 8, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_all_gather(outs, 2, _tab(A + 8194, A + 8192), 8, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_all_gather(outs, 2, parts, 0, None) == S["DETFOLD_OK"]
+
+
+@no_gpu_only
 def test_validation_scale_and_floor(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_scale(None, 8, 0.5, None) == S["DETFOLD_ERR_NULL"]
@@ -164,16 +203,7 @@ def test_validation_scale_and_floor(df):
     assert L.detfold_launch_floor(0, 1, None) == S["DETFOLD_OK"]
 
 
-def _has_gpu():
-    try:
-        import torch
-        return torch.cuda.is_available()
-    except Exception:
-        return True  # unknown: assume a GPU and skip
-
-
-@pytest.mark.skipif(_has_gpu() or os.path.exists("/dev/nvidia0"),
-                    reason="only meaningful (and only safe) where no GPU exists")
+@no_gpu_only
 def test_launch_without_device_reports_cuda_error(df):
     L, S = df.lib, df.STATUS
     rc = L.detfold_sum_stacked(A, A + 4096, 2, 8, None)

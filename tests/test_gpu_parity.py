@@ -167,7 +167,7 @@ def test_c5_stress_sum_mean_and_allreduce(W, variant):
     assert buf.intact()
     assert_bitwise(buf.host(), mean_want, f"C5 mean W={W}")
     # fused all-reduce with the mean in registers, and the staged comparator
-    for flags in (None, 0, 1, 2, 3):
+    for flags in (None, 0, 1, 2, 3, 4):
         ar = run_allreduce(rows, float(m), offs, staged_flags=flags)
         for r in range(W):
             assert_bitwise(ar[r], mean_want, f"C5 all-reduce W={W} flags={flags} rank={r}")
@@ -222,7 +222,7 @@ def test_allreduce_fused_and_staged_match_oracle(W, n):
     rows = gen.normal_rows(W, n)
     for scale in (1.0, float(oracle.mean_scale(W))):
         exp = oracle_allreduce(rows, scale)
-        for flags in (None, 0, 1, 2, 3):
+        for flags in (None, 0, 1, 2, 3, 4, 7):
             got = run_allreduce(rows, scale, staged_flags=flags)
             for r in range(W):
                 assert_bitwise(got[r], exp[r], f"W={W} n={n} scale={scale} flags={flags} r={r}")
@@ -251,6 +251,53 @@ def test_len_zero_and_one_rank_are_noops():
     sync()
     assert_bitwise(a.host(), np.arange(16, dtype=np.float32), "no-op calls changed data")
     assert a.intact()
+
+
+# ------------------------------------------------------------------ pure movement
+
+def _random_bits(n, seed):
+    # every 32-bit pattern is fair game for movement: NaN payloads, -0, subnormals
+    return np.random.default_rng(seed).integers(0, 2 ** 32, size=n, dtype=np.uint64) \
+        .astype(np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("span", [1, 1024, 16384, (1 << 20) + 3])
+@pytest.mark.parametrize("W", [2, 3, 8])
+def test_broadcast_and_all_gather_move_bytes_exactly(span, W):
+    # broadcast: the root's buffer lands on every other rank byte for byte
+    src_h = _random_bits(span, 31 + span)
+    src = Guarded(span, 3, src_h)
+    dsts = [Guarded(span, 3 if r % 2 else 0) for r in range(W - 1)]
+    df.detfold_broadcast([d.t for d in dsts], W - 1, src.t, span)
+    sync()
+    for k, d in enumerate(dsts):
+        assert_bitwise(d.host(), src_h, f"broadcast span={span} dst={k}")
+        assert d.intact()
+    assert src.intact()
+    assert_bitwise(src.host(), src_h, "broadcast source modified")
+    # all-gather: rank-order concatenation, identical on every rank
+    parts_h = [_random_bits(span, 41 + r + span) for r in range(W)]
+    parts = [Guarded(span, r % 2, parts_h[r]) for r in range(W)]
+    outs = [Guarded(W * span, (r * 5) % 8) for r in range(W)]
+    df.detfold_all_gather([o.t for o in outs], W, [p.t for p in parts], span)
+    sync()
+    want = np.concatenate(parts_h)
+    for r, o in enumerate(outs):
+        assert_bitwise(o.host(), want, f"all-gather span={span} rank={r}")
+        assert o.intact()
+
+
+def test_broadcast_many_destinations_splits_launches():
+    # more destinations than one parameter block holds
+    span, nd = 1000, 256
+    src_h = _random_bits(span, 7)
+    src = Guarded(span, 0, src_h)
+    dsts = [Guarded(span, r % 8) for r in range(nd)]
+    df.detfold_broadcast([d.t for d in dsts], nd, src.t, span)
+    sync()
+    for d in dsts:
+        assert_bitwise(d.host(), src_h, "broadcast to 256")
+        assert d.intact()
 
 
 # ------------------------------------------------------------------ C2: small payload + graphs
@@ -349,7 +396,8 @@ def test_c4_full_size_w4_fused_and_staged_bitwise():
     del fused
     nb = df.detfold_staged_workspace_bytes(n, W)
     ws = torch.empty(nb // 4, dtype=torch.float32, device="cuda")
-    for flags in (0, df.DETFOLD_STAGED_SEPARATE_SCALE | df.DETFOLD_STAGED_REVERSE_DELIVERY):
+    for flags in (0, df.DETFOLD_STAGED_SEPARATE_SCALE | df.DETFOLD_STAGED_REVERSE_DELIVERY,
+                  df.DETFOLD_STAGED_CE_COPIES):
         staged = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
         df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, flags, ws, nb)
         sync()

@@ -501,60 +501,73 @@ def run_gpu(args) -> None:
 
     graph = {n: graph_us_per_call(torch, df, wl, n) for n in C2_NS}
 
-    # end to end through the public API with host buffers: every step copies
-    # its inputs from pinned host memory, runs every row, and reads back
-    # every result.
+    # End to end through the public API with host buffers: every step copies
+    # each row's inputs from pinned host memory, runs the row, and reads back
+    # every result. Three streams pipeline the rows: uploads run ahead on an
+    # H2D stream, the calls run on the compute stream as each row's inputs
+    # land, and results drain on a D2H stream, so the two link directions
+    # overlap. Events keep a buffer from being overwritten before the previous
+    # step has finished reading it.
     e2e_steps = max(3, min(20, K))
-    h_out = {
-        "c3": torch.empty(C3_N, dtype=torch.float32, pin_memory=True),
-        "c3b": torch.empty(C3_N, dtype=torch.float32, pin_memory=True),
-        "c4f": torch.empty(C4_W * C4_N, dtype=torch.float32, pin_memory=True),
-        "c4s": torch.empty(C4_W * C4_N, dtype=torch.float32, pin_memory=True),
+    pin = lambda n: torch.empty(n, dtype=torch.float32, pin_memory=True)
+    h_out = {"c3": pin(C3_N), "c3b": pin(C3_N), "c4f": pin(C4_W * C4_N), "c4s": pin(C4_W * C4_N)}
+    for W in C5_WS:
+        h_out[f"c5s{W}"] = pin(C5_N)
+        h_out[f"c5a{W}"] = pin(W * C5_N)
+    for n in C2_NS:
+        h_out[f"c2{n}"] = pin(n)
+    # (row name, [(device dst, host src)], [(host dst, device src)])
+    io = {
+        "c3_stacked": ([(wl.c3, wl.h_c3)], [(h_out["c3"], wl.c3_out)]),
+        "c3_ptrs": ([], [(h_out["c3b"], wl.c3_out2)]),
+        "c4_fused": ([(wl.c4f[r], wl.h_c4[r * C4_N:(r + 1) * C4_N]) for r in range(C4_W)],
+                     [(h_out["c4f"][r * C4_N:(r + 1) * C4_N], wl.c4f[r]) for r in range(C4_W)]),
+        "c4_staged": ([(wl.c4s[r], wl.h_c4[r * C4_N:(r + 1) * C4_N]) for r in range(C4_W)],
+                      [(h_out["c4s"][r * C4_N:(r + 1) * C4_N], wl.c4s[r]) for r in range(C4_W)]),
     }
     for W in C5_WS:
-        h_out[f"c5s{W}"] = torch.empty(C5_N, dtype=torch.float32, pin_memory=True)
-        h_out[f"c5a{W}"] = torch.empty(W * C5_N, dtype=torch.float32, pin_memory=True)
+        ins, outs = [], [(h_out[f"c5s{W}"], wl.c5_out[W])]
+        for r in range(W):
+            src = wl.h_c5[W][r * C5_N:(r + 1) * C5_N]
+            ins += [(wl.c5_sum_src[W][r], src), (wl.c5_ar[W][r], src)]
+            outs.append((h_out[f"c5a{W}"][r * C5_N:(r + 1) * C5_N], wl.c5_ar[W][r]))
+        io[f"c5_w{W}"] = (ins, outs)
     for n in C2_NS:
-        h_out[f"c2{n}"] = torch.empty(n, dtype=torch.float32, pin_memory=True)
-    h2d = d2h = 0
+        io[f"c2_{n}"] = ([(wl.c2[n], wl.h_c2[n])], [(h_out[f"c2{n}"], wl.c2_out[n])])
+    h2d = sum(d.numel() * 4 for ins, _ in io.values() for d, _ in ins)
+    d2h = sum(h.numel() * 4 for _, outs in io.values() for h, _ in outs)
+    s_h2d = torch.cuda.Stream(device=dev)
+    s_d2h = torch.cuda.Stream(device=dev)
+    s_cmp = torch.cuda.Stream(device=dev)
+    ev_cmp = {name: None for name, _, _ in rows}
+    ev_d2h = {name: None for name, _, _ in rows}
+    # rows that also read a row's uploaded inputs (c3_ptrs folds the C3 rows)
+    also_reads = {"c3_stacked": ["c3_ptrs"]}
 
     def e2e_step():
-        nonlocal h2d, d2h
-        h2d = d2h = 0
-        wl.c3.copy_(wl.h_c3, non_blocking=True)
-        h2d += wl.h_c3.numel() * 4
-        for r in range(C4_W):
-            src = wl.h_c4[r * C4_N:(r + 1) * C4_N]
-            wl.c4f[r].copy_(src, non_blocking=True)
-            wl.c4s[r].copy_(src, non_blocking=True)
-            h2d += 2 * C4_N * 4
-        for W in C5_WS:
-            for r in range(W):
-                src = wl.h_c5[W][r * C5_N:(r + 1) * C5_N]
-                wl.c5_sum_src[W][r].copy_(src, non_blocking=True)
-                wl.c5_ar[W][r].copy_(src, non_blocking=True)
-                h2d += 2 * C5_N * 4
-        for n in C2_NS:
-            wl.c2[n].copy_(wl.h_c2[n], non_blocking=True)
-            h2d += 2 * n * 4
-        for _, fn, _ in rows:
-            fn()
-        h_out["c3"].copy_(wl.c3_out, non_blocking=True)
-        h_out["c3b"].copy_(wl.c3_out2, non_blocking=True)
-        d2h += 2 * C3_N * 4
-        for r in range(C4_W):
-            h_out["c4f"][r * C4_N:(r + 1) * C4_N].copy_(wl.c4f[r], non_blocking=True)
-            h_out["c4s"][r * C4_N:(r + 1) * C4_N].copy_(wl.c4s[r], non_blocking=True)
-            d2h += 2 * C4_N * 4
-        for W in C5_WS:
-            h_out[f"c5s{W}"].copy_(wl.c5_out[W], non_blocking=True)
-            d2h += C5_N * 4
-            for r in range(W):
-                h_out[f"c5a{W}"][r * C5_N:(r + 1) * C5_N].copy_(wl.c5_ar[W][r], non_blocking=True)
-                d2h += C5_N * 4
-        for n in C2_NS:
-            h_out[f"c2{n}"].copy_(wl.c2_out[n], non_blocking=True)
-            d2h += n * 4
+        for name, fn, _ in rows:
+            ins, outs = io[name]
+            with torch.cuda.stream(s_h2d):
+                for ev in [ev_cmp[name], ev_d2h[name]] + [ev_cmp[x] for x in also_reads.get(name, [])]:
+                    if ev is not None:
+                        s_h2d.wait_event(ev)
+                for d, h in ins:
+                    d.copy_(h, non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(s_h2d)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(landed)
+                if ev_d2h[name] is not None:
+                    s_cmp.wait_event(ev_d2h[name])
+                fn()
+                ev_cmp[name] = torch.cuda.Event()
+                ev_cmp[name].record(s_cmp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_cmp[name])
+                for h, d in outs:
+                    h.copy_(d, non_blocking=True)
+                ev_d2h[name] = torch.cuda.Event()
+                ev_d2h[name].record(s_d2h)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -563,10 +576,16 @@ def run_gpu(args) -> None:
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    e0.record(stream)
+    e0.record(s_h2d)
+    s_cmp.wait_event(e0)
+    s_d2h.wait_event(e0)
     for _ in range(e2e_steps):
         e2e_step()
-    e1.record(stream)
+    for st_ in (s_h2d, s_cmp):
+        done = torch.cuda.Event()
+        done.record(st_)
+        s_d2h.wait_event(done)
+    e1.record(s_d2h)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if dist:
@@ -574,11 +593,17 @@ def run_gpu(args) -> None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
-    # the read-back of the last end-to-end step is one step from the inputs
+    # every step starts from the host inputs, so the read-back is one step
     e2e_check = 0
     idx = np.arange(0, C3_N, 16411)
     want3 = oracle.fold_stacked(np.ascontiguousarray(wl.h_c3.numpy().reshape(C3_W, C3_N)[:, idx]))
     e2e_check += oracle.bit_diffs(h_out["c3"].numpy()[idx], want3)
+    idx4 = np.arange(0, C4_N, 24593)
+    ar = [np.ascontiguousarray(wl.h_c4.numpy().reshape(C4_W, C4_N)[r, idx4]) for r in range(C4_W)]
+    oracle.allreduce(ar, np.float32(wl.scale4))
+    for r in range(C4_W):
+        e2e_check += oracle.bit_diffs(h_out["c4f"].numpy()[r * C4_N + idx4], ar[r])
+        e2e_check += oracle.bit_diffs(h_out["c4s"].numpy()[r * C4_N + idx4], ar[r])
 
     if rank != 0:
         if dist:
@@ -619,6 +644,7 @@ def run_gpu(args) -> None:
         "bitwise_sampled": check,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "pipelined": "H2D, compute and D2H on three streams, rows overlapped",
                 "bitwise_sampled_words_differing": int(e2e_check)},
         "gpu_launches": launches,
         "clocks": clock_summary,

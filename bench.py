@@ -58,7 +58,15 @@ GRAPH_NODES = 10_000
 
 # DRAM traffic of the dominant kernel from one ncu capture, keyed by a hash of
 # the kernel sources it was taken on; null once the kernel has changed.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/fold_vec_kernel_W8_stacked.md: full-size C3 launch (8 x 2^26),
+    # dram__bytes_read.sum + dram__bytes_write.sum
+    "fold_vec_kernel<W=8,kSumNC>": {"bytes_per_launch": 2150019072 + 261127424,
+                                    "kernel_hash": "60ca0eb98dfe56ad"},
+    # profiles/fold_vec_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
+    "fold_vec_kernel<W=4,kAllReduce>": {"bytes_per_launch": 1600070144 + 1538395904,
+                                        "kernel_hash": "60ca0eb98dfe56ad"},
+}
 
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "fold_sum_nc.cu",
@@ -100,6 +108,22 @@ def peaks() -> tuple[float, str]:
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: every rank runs its own replica, the job is
+    done when the last one is."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, step_bytes: int, ms_per_step: float) -> float:
+    """All ranks' algorithmic bytes over the slowest rank's step time."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------------ clocks
@@ -320,6 +344,20 @@ def graph_us_per_call(torch, df, wl, n: int, reps: int = 25) -> dict:
     g = capture(folds)
     res["us_per_call"] = time_graph(g)
     del g
+    # the same fold through a device-resident pointer table (rebindable)
+    rows2 = [wl.c2[n][:n], wl.c2[n][n:]]
+    table = df.device_table(rows2)
+    with torch.cuda.stream(stream):
+        df.detfold_sum_ptrs_dev(wl.c2_out[n], table, 2, n)
+    stream.synchronize()
+
+    def table_folds():
+        for _ in range(GRAPH_NODES):
+            df.detfold_sum_ptrs_dev(wl.c2_out[n], table, 2, n)
+
+    g = capture(table_folds)
+    res["us_per_call_device_table"] = time_graph(g)
+    del g
     g = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 1))
     res["floor_us_pdl"] = time_graph(g)
     del g
@@ -327,6 +365,43 @@ def graph_us_per_call(torch, df, wl, n: int, reps: int = 25) -> dict:
     res["floor_us_plain"] = time_graph(g)
     del g
     return res
+
+
+def next_rows(torch, df, wl, reps: int = 10) -> dict:
+    """Rows beyond the step: pure-movement broadcast and all-gather, and the
+    fold over a device-resident pointer table, in algorithmic GB/s."""
+    def t(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+    out = {}
+    # broadcast: C3 row 0 to the other seven rows' worth of space (reads 1, writes 7)
+    dsts = [torch.empty(C3_N, dtype=torch.float32, device=wl.dev) for _ in range(7)]
+    ms = t(lambda: df.detfold_broadcast(dsts, 7, wl.c3_rows[0], C3_N))
+    out["broadcast_1to7_2^26"] = {"ms": round(ms, 4), "gbs": round(8 * C3_N * 4 / (ms * 1e-3) / 1e9, 1)}
+    del dsts
+    span, W = 1 << 24, 4
+    outs = [torch.empty(W * span, dtype=torch.float32, device=wl.dev) for _ in range(W)]
+    parts = [wl.c3_rows[r][:span] for r in range(W)]
+    ms = t(lambda: df.detfold_all_gather(outs, W, parts, span))
+    out["all_gather_W4_2^24"] = {"ms": round(ms, 4),
+                                 "gbs": round((W + W * W) * span * 4 / (ms * 1e-3) / 1e9, 1)}
+    del outs
+    table = df.device_table(wl.c3_rows)
+    ms = t(lambda: df.detfold_sum_ptrs_dev(wl.c3_out2, table, C3_W, C3_N))
+    out["sum_ptrs_dev_W8_2^26"] = {"ms": round(ms, 4),
+                                   "gbs": round((C3_W + 1) * C3_N * 4 / (ms * 1e-3) / 1e9, 1)}
+    return out
 
 
 def copy_peak_gbs(torch, dev) -> float:
@@ -457,13 +532,9 @@ def run_gpu(args) -> None:
         if dist:
             dist.barrier()
     clock_summary = clk.summary()
-    ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_per_step = ms / K
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, ms_per_step)
 
     per_row = {}
     launches = 0
@@ -500,6 +571,7 @@ def run_gpu(args) -> None:
     check = sampled_check(wl, steps_done, torch, oracle, rng)
 
     graph = {n: graph_us_per_call(torch, df, wl, n) for n in C2_NS}
+    extra_rows = next_rows(torch, df, wl)
 
     # End to end through the public API with host buffers: every step copies
     # each row's inputs from pinned host memory, runs the row, and reads back
@@ -587,12 +659,8 @@ def run_gpu(args) -> None:
         s_d2h.wait_event(done)
     e1.record(s_d2h)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e_value = whole_job_gbs(world, step_bytes, e2e_ms)
     # every step starts from the host inputs, so the read-back is one step
     e2e_check = 0
     idx = np.arange(0, C3_N, 16411)
@@ -640,6 +708,7 @@ def run_gpu(args) -> None:
         "rows": per_row,
         "roofline": roofline,
         "c2_graph": {str(n): {k: round(v, 3) for k, v in graph[n].items()} for n in C2_NS},
+        "next_rows": extra_rows,
         "copy_peak_gbs_this_run": round(copy_gbs, 1),
         "bitwise_sampled": check,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,

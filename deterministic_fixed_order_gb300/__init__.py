@@ -22,7 +22,8 @@ from . import build as _build
 __all__ = [
     "DetfoldError", "lib", "DETFOLD_MAX_W", "DETFOLD_MAX_LEN",
     "DETFOLD_STAGED_REVERSE_DELIVERY", "DETFOLD_STAGED_SEPARATE_SCALE", "DETFOLD_STAGED_CE_COPIES",
-    "detfold_broadcast", "detfold_all_gather",
+    "detfold_broadcast", "detfold_all_gather", "detfold_sum_ptrs_dev",
+    "detfold_loopback_allreduce_dev", "device_table",
     "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
     "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
     "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_noalloc",
@@ -66,6 +67,8 @@ lib.detfold_staged_workspace_bytes.restype = _I64
 lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _INT, _P, _I64, _P]
 lib.detfold_loopback_allreduce_staged_noalloc.argtypes = [_P, _INT, _I64, _F, _INT, _P]
 lib.detfold_broadcast.argtypes = [_P, _INT, _P, _I64, _P]
+lib.detfold_sum_ptrs_dev.argtypes = [_P, _P, _INT, _I64, _P, _P]
+lib.detfold_loopback_allreduce_dev.argtypes = [_P, _INT, _I64, _F, _P, _P]
 lib.detfold_all_gather.argtypes = [_P, _INT, _P, _I64, _P]
 lib.detfold_shard_plan.argtypes = [_I64, _INT, _P, _P]
 lib.detfold_status_string.argtypes = [_INT]
@@ -75,6 +78,7 @@ lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
 for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
               "detfold_loopback_allreduce_staged_noalloc", "detfold_broadcast",
+              "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
               "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
     getattr(lib, _name).restype = _INT
 
@@ -181,6 +185,47 @@ def status_all_gather(outs, W: int, parts, span: int, stream=None) -> int:
     return lib.detfold_all_gather(otab, W, ptab, span, _stream(stream))
 
 
+def _table_ptr(table, W: int) -> int:
+    """Address of a device pointer table: a CUDA int64 tensor of >= W entries, or an int."""
+    if isinstance(table, int):
+        return table
+    import torch
+    if not isinstance(table, torch.Tensor) or not table.is_cuda or table.dtype != torch.int64:
+        raise TypeError("table: expected a CUDA int64 tensor of device addresses")
+    if not table.is_contiguous() or table.numel() < W:
+        raise ValueError(f"table: needs {W} contiguous entries, has {table.numel()}")
+    return table.data_ptr()
+
+
+def _status_ptr(status) -> int:
+    if status is None or isinstance(status, int):
+        return status or 0
+    import torch
+    if not status.is_cuda or status.dtype != torch.int32 or status.numel() < 1:
+        raise TypeError("status: expected a CUDA int32 tensor")
+    return status.data_ptr()
+
+
+def device_table(tensors, device=None):
+    """A CUDA int64 tensor holding the data addresses of `tensors` (for the
+    *_dev entry points). Each tensor must be a CUDA float32 tensor."""
+    import torch
+    ptrs = [_dev_ptr(t, None, f"tensors[{k}]") for k, t in enumerate(tensors)]
+    dev = device if device is not None else tensors[0].device
+    return torch.tensor(ptrs, dtype=torch.int64, device=dev)
+
+
+def status_sum_ptrs_dev(out, table, W: int, length: int, status=None, stream=None) -> int:
+    return lib.detfold_sum_ptrs_dev(_dev_ptr(out, length, "out"), _table_ptr(table, W), W, length,
+                                    _status_ptr(status), _stream(stream))
+
+
+def status_loopback_allreduce_dev(table, W: int, length: int, mean_scale: float = 1.0,
+                                  status=None, stream=None) -> int:
+    return lib.detfold_loopback_allreduce_dev(_table_ptr(table, W), W, length, mean_scale,
+                                              _status_ptr(status), _stream(stream))
+
+
 # ------------------------------------------------------------------ raising calls (C names)
 
 def detfold_sum_stacked(out, stacked, W: int, length: int, stream=None) -> None:
@@ -226,6 +271,19 @@ def detfold_loopback_allreduce_staged_noalloc(arenas, W: int, length: int,
     the shared scratch."""
     _check(status_loopback_allreduce_staged_noalloc(arenas, W, length, mean_scale, flags, stream),
            "detfold_loopback_allreduce_staged_noalloc")
+
+
+def detfold_sum_ptrs_dev(out, table, W: int, length: int, status=None, stream=None) -> None:
+    """Fold over a device-resident pointer table (see include/detfold.h).
+    The table's entries are not visible to the host: they must address
+    `length` floats each, as the caller guarantees."""
+    _check(status_sum_ptrs_dev(out, table, W, length, status, stream), "detfold_sum_ptrs_dev")
+
+
+def detfold_loopback_allreduce_dev(table, W: int, length: int, mean_scale: float = 1.0,
+                                   status=None, stream=None) -> None:
+    _check(status_loopback_allreduce_dev(table, W, length, mean_scale, status, stream),
+           "detfold_loopback_allreduce_dev")
 
 
 def detfold_broadcast(dsts, ndst: int, src, length: int, stream=None) -> None:

@@ -325,6 +325,33 @@ int detfold_all_gather(float *const *outs, int W, const float *const *parts, int
     return DETFOLD_OK;
 }
 
+int detfold_sum_ptrs_dev(float *out, const float *const *d_srcs, int W, int64_t len, int *d_status,
+                         void *stream)
+{
+    if (!out || !d_srcs) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    if (!aligned4(out) || ((uintptr_t)d_srcs & 7u) || ((uintptr_t)d_status & 3u))
+        return DETFOLD_ERR_ALIGN;
+    if (len == 0) return DETFOLD_OK;
+    return cuda_status(detfold::launch_table(d_srcs, out, d_status, W, len, 1.0f, 0,
+                                             detfold::kSumCoherent, (cudaStream_t)stream));
+}
+
+int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, float mean_scale,
+                                   int *d_status, void *stream)
+{
+    if (!d_arenas) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    if (int rc = check_len(len)) return rc;
+    if (((uintptr_t)d_arenas & 7u) || ((uintptr_t)d_status & 3u)) return DETFOLD_ERR_ALIGN;
+    const int do_scale = mean_scale != 1.0f;
+    if (len == 0 || (W == 1 && !do_scale)) return DETFOLD_OK;
+    return cuda_status(detfold::launch_table((const float *const *)d_arenas, nullptr, d_status, W,
+                                             len, mean_scale, do_scale, detfold::kAllReduce,
+                                             (cudaStream_t)stream));
+}
+
 int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens)
 {
     if (!starts || !lens) return DETFOLD_ERR_NULL;

@@ -65,10 +65,11 @@ inline constexpr int u_for(int W, int vec)
     return u < 1 ? 1 : u;
 }
 
-// Resident CTAs the whole GPU holds for `kernel` at `threads` per CTA,
-// computed once per (instantiation, device).
-template <typename Kernel>
-inline cudaError_t resident_ctas(Kernel kernel, int threads, int cap_per_sm, int *out)
+// Resident CTAs the whole GPU holds for `Kernel` at `threads` per CTA (at
+// most cap_per_sm per SM when cap_per_sm > 0). Computed once per kernel and
+// device: the cache lives in this function's instantiation for that kernel.
+template <auto Kernel>
+inline cudaError_t resident_ctas(int threads, int cap_per_sm, int *out)
 {
     static std::atomic<int> cache[64];
     int dev = 0;
@@ -80,7 +81,7 @@ inline cudaError_t resident_ctas(Kernel kernel, int threads, int cap_per_sm, int
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kernel, threads, 0);
         if (e != cudaSuccess) return e;
         if (cap_per_sm > 0 && per_sm > cap_per_sm) per_sm = cap_per_sm;
         v = sms * (per_sm > 0 ? per_sm : 1);
@@ -90,9 +91,12 @@ inline cudaError_t resident_ctas(Kernel kernel, int threads, int cap_per_sm, int
     return cudaSuccess;
 }
 
-template <typename Params>
-inline cudaError_t launch_kernel(void (*kernel)(Params), const Params &p, int64_t work, int u,
-                                 bool small, int bw_threads, int cap_per_sm, cudaStream_t stream)
+// One launch: the small path covers the work exactly with small CTAs and
+// programmatic dependent launch; the bandwidth path runs a grid of at most
+// the resident CTAs, each thread striding over U-vector groups.
+template <auto Kernel, typename Params>
+inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool small, int bw_threads,
+                                 int cap_per_sm, cudaStream_t stream)
 {
     const int threads = small ? DETFOLD_SMALL_THREADS : bw_threads;
     int64_t blocks = (work + threads - 1) / threads;
@@ -100,7 +104,7 @@ inline cudaError_t launch_kernel(void (*kernel)(Params), const Params &p, int64_
         const int64_t per_iter = (int64_t)threads * u;
         blocks = (work + per_iter - 1) / per_iter;
         int cap = 0;
-        const cudaError_t e = resident_ctas(kernel, threads, cap_per_sm, &cap);
+        const cudaError_t e = resident_ctas<Kernel>(threads, cap_per_sm, &cap);
         if (e != cudaSuccess) return e;
         if (blocks > cap) blocks = cap;
     }
@@ -118,7 +122,7 @@ inline cudaError_t launch_kernel(void (*kernel)(Params), const Params &p, int64_
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kernel, p);
+    return cudaLaunchKernelEx(&cfg, Kernel, p);
 }
 
 template <int NT>
@@ -147,14 +151,14 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
     constexpr int C = ctas_per_sm_cap<MODE>();
     if (pl.vec == 8) {
         constexpr int U = u_for<MODE>(W, 8);
-        return launch_kernel(fold_vec_kernel<W, 8, U, MODE>, p, pl.nvec, U, small, T, C, stream);
+        return launch_kernel<fold_vec_kernel<W, 8, U, MODE>>(p, pl.nvec, U, small, T, C, stream);
     }
     if (pl.vec == 4) {
         constexpr int U = u_for<MODE>(W, 4);
-        return launch_kernel(fold_vec_kernel<W, 4, U, MODE>, p, pl.nvec, U, small, T, C, stream);
+        return launch_kernel<fold_vec_kernel<W, 4, U, MODE>>(p, pl.nvec, U, small, T, C, stream);
     }
     constexpr int U = u_for<MODE>(W, 0);
-    return launch_kernel(fold_scalar_kernel<W, U, MODE>, p, s.len, U, small, T, C, stream);
+    return launch_kernel<fold_scalar_kernel<W, U, MODE>>(p, s.len, U, small, T, C, stream);
 }
 
 template <int MODE>
@@ -165,9 +169,9 @@ inline cudaError_t launch_generic(const LaunchSpec &s, cudaStream_t stream)
     const FoldParams<kGenericW> p = fill_params<kGenericW>(s, pl, small);
     constexpr int T = bw_threads<MODE>();
     constexpr int C = ctas_per_sm_cap<MODE>();
-    if (pl.vec == 8) return launch_kernel(fold_vec_generic_kernel<8, MODE>, p, pl.nvec, 1, small, T, C, stream);
-    if (pl.vec == 4) return launch_kernel(fold_vec_generic_kernel<4, MODE>, p, pl.nvec, 1, small, T, C, stream);
-    return launch_kernel(fold_scalar_generic_kernel<MODE>, p, s.len, 1, small, T, C, stream);
+    if (pl.vec == 8) return launch_kernel<fold_vec_generic_kernel<8, MODE>>(p, pl.nvec, 1, small, T, C, stream);
+    if (pl.vec == 4) return launch_kernel<fold_vec_generic_kernel<4, MODE>>(p, pl.nvec, 1, small, T, C, stream);
+    return launch_kernel<fold_scalar_generic_kernel<MODE>>(p, s.len, 1, small, T, C, stream);
 }
 
 template <int MODE>
@@ -192,6 +196,9 @@ cudaError_t launch_sum_nc(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_sum_coherent(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_allreduce(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_empty(int count, int pdl, cudaStream_t stream);
+// Fold or all-reduce over a device-resident pointer table (fold_table.cu).
+cudaError_t launch_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
+                         float scale, int do_scale, int mode, cudaStream_t stream);
 // Pure movement of K pairs (move_kernels.cu); K may exceed kMaxPairs.
 cudaError_t launch_move(const float *const *src, float *const *dst, int K, int64_t len,
                         cudaStream_t stream);

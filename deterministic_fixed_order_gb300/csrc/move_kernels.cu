@@ -103,9 +103,9 @@ static cudaError_t launch_move_chunk(const float *const *src, float *const *dst,
             break;
         }
     }
-    if (vec == 8) return launch_kernel(move_pairs_kernel<8>, p, p.nvec, 1, small, 256, 0, stream);
-    if (vec == 4) return launch_kernel(move_pairs_kernel<4>, p, p.nvec, 1, small, 256, 0, stream);
-    return launch_kernel(move_pairs_scalar_kernel, p, len, 1, small, 256, 0, stream);
+    if (vec == 8) return launch_kernel<move_pairs_kernel<8>>(p, p.nvec, 1, small, 256, 0, stream);
+    if (vec == 4) return launch_kernel<move_pairs_kernel<4>>(p, p.nvec, 1, small, 256, 0, stream);
+    return launch_kernel<move_pairs_scalar_kernel>(p, len, 1, small, 256, 0, stream);
 }
 
 cudaError_t launch_move(const float *const *src, float *const *dst, int K, int64_t len,

@@ -146,6 +146,34 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
                                       int64_t workspace_bytes, void *stream);
 
 /*
+ * Pointer-table fold with the table in device memory. The kernel reads the
+ * table when it runs, so a CUDA graph captured once follows new addresses
+ * written into the table between replays (the rebind pattern of
+ * memra-engine 0.136.0 tests/gdn_packed_gpu.rs, `packed_matches_per_row`
+ * with graph_rebind). Same chain and bits as detfold_sum_ptrs.
+ *   out       device, len f32, written; may be one of the sources.
+ *   d_srcs    DEVICE array of W device pointers (8-byte aligned), read by the
+ *             kernel; each entry must address len f32 that stay valid until
+ *             the launch completes. Only the out == srcs[k] overlap is legal;
+ *             the host cannot check this, so it is the caller's contract.
+ *   d_status  optional DEVICE int (NULL = none): set to DETFOLD_OK, or to
+ *             DETFOLD_ERR_NULL / DETFOLD_ERR_ALIGN when a table entry is NULL
+ *             or not 4-byte aligned -- then nothing else is written. Not
+ *             touched when the call returns before launching (len == 0 or
+ *             a host-side error).
+ */
+int detfold_sum_ptrs_dev(float *out, const float *const *d_srcs, int W, int64_t len, int *d_status,
+                         void *stream);
+
+/*
+ * Fused loopback all-reduce over a device-resident arena table (as
+ * detfold_loopback_allreduce, with the table read by the kernel; arenas must
+ * be pairwise disjoint -- the caller's contract). d_status as above.
+ */
+int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, float mean_scale,
+                                   int *d_status, void *stream);
+
+/*
  * Broadcast, pure byte movement (memra-engine 0.128.0 tests/tp_ar_gpu.rs,
  * `broadcast_and_all_gather_move_bytes_exactly`: rank 0's buffer lands on
  * every other rank byte for byte): dsts[k][i] = src[i] for every k.

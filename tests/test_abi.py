@@ -193,6 +193,25 @@ def test_validation_broadcast_and_all_gather(df):
 
 
 @no_gpu_only
+def test_validation_device_tables(df):
+    L, S = df.lib, df.STATUS
+    T = A + (1 << 16)  # a fake 8-byte-aligned device table address
+    assert L.detfold_sum_ptrs_dev(None, T, 2, 8, None, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_sum_ptrs_dev(A, None, 2, 8, None, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_sum_ptrs_dev(A, T, 0, 8, None, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_sum_ptrs_dev(A, T, 2, -2, None, None) == S["DETFOLD_ERR_LEN"]
+    assert L.detfold_sum_ptrs_dev(A, T + 4, 2, 8, None, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_sum_ptrs_dev(A + 2, T, 2, 8, None, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_sum_ptrs_dev(A, T, 2, 8, A + 6, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_sum_ptrs_dev(A, T, 2, 0, None, None) == S["DETFOLD_OK"]
+    assert L.detfold_loopback_allreduce_dev(None, 2, 8, 1.0, None, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_loopback_allreduce_dev(T, 300, 8, 1.0, None, None) == S["DETFOLD_ERR_WORLD"]
+    assert L.detfold_loopback_allreduce_dev(T + 2, 2, 8, 1.0, None, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_loopback_allreduce_dev(T, 1, 8, 1.0, None, None) == S["DETFOLD_OK"]
+    assert L.detfold_loopback_allreduce_dev(T, 2, 0, 0.5, None, None) == S["DETFOLD_OK"]
+
+
+@no_gpu_only
 def test_validation_scale_and_floor(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_scale(None, 8, 0.5, None) == S["DETFOLD_ERR_NULL"]

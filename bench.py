@@ -397,6 +397,33 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
     out["all_gather_W4_2^24"] = {"ms": round(ms, 4),
                                  "gbs": round((W + W * W) * span * 4 / (ms * 1e-3) / 1e9, 1)}
     del outs
+    # one-shot emulation at the decode-join size, per-call device time
+    n = 4096
+    arenas = [wl.c2[n][:n].clone(), wl.c2[n][n:].clone()]
+    link = df.OneShotLink(2, n, device=wl.dev)
+
+    def per_call_us(fn, calls=200):
+        ts = []
+        for _ in range(calls):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+    for _ in range(5):
+        link.all_reduce(arenas)
+
+    def one_shot():
+        link.epoch += 1
+        df.detfold_one_shot_allreduce(arenas, 2, n, 1.0, link.link, link.epoch, link.stage,
+                                      link.words)
+    out["one_shot_W2_16KiB_us_per_call"] = round(per_call_us(one_shot), 2)
+    out["one_shot_barrier_errors"] = link.barrier_errors()
+    out["fused_W2_16KiB_us_per_call_same_timing"] = round(
+        per_call_us(lambda: df.detfold_loopback_allreduce(arenas, 2, n, 1.0)), 2)
     table = df.device_table(wl.c3_rows)
     ms = t(lambda: df.detfold_sum_ptrs_dev(wl.c3_out2, table, C3_W, C3_N))
     out["sum_ptrs_dev_W8_2^26"] = {"ms": round(ms, 4),

@@ -23,7 +23,7 @@ __all__ = [
     "DetfoldError", "lib", "DETFOLD_MAX_W", "DETFOLD_MAX_LEN",
     "DETFOLD_STAGED_REVERSE_DELIVERY", "DETFOLD_STAGED_SEPARATE_SCALE", "DETFOLD_STAGED_CE_COPIES",
     "detfold_broadcast", "detfold_all_gather", "detfold_sum_ptrs_dev",
-    "detfold_loopback_allreduce_dev", "device_table",
+    "detfold_loopback_allreduce_dev", "device_table", "detfold_one_shot_allreduce", "OneShotLink",
     "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
     "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
     "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_noalloc",
@@ -45,6 +45,11 @@ STATUS = {
     "DETFOLD_ERR_CUDA": -7, "DETFOLD_ERR_ARG": -8, "DETFOLD_ERR_SCRATCH_LIMIT": -9,
 }
 DETFOLD_NOALLOC_SCRATCH_BYTES = 16 << 20
+DETFOLD_ONESHOT_MAX_W = 64
+DETFOLD_ONESHOT_MAX_LEN = 1 << 22
+DETFOLD_ONESHOT_LINK_BYTES = 2 * 1024 * 8
+DETFOLD_ONESHOT_REFUSE_ENTRY = 40043
+DETFOLD_ONESHOT_REFUSE_EXIT = 40044
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -68,6 +73,8 @@ lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _INT, _P, 
 lib.detfold_loopback_allreduce_staged_noalloc.argtypes = [_P, _INT, _I64, _F, _INT, _P]
 lib.detfold_broadcast.argtypes = [_P, _INT, _P, _I64, _P]
 lib.detfold_sum_ptrs_dev.argtypes = [_P, _P, _INT, _I64, _P, _P]
+lib.detfold_one_shot_allreduce.argtypes = [_P, _INT, _I64, _F, _P, ctypes.c_uint64, _P, _P, _I64,
+                                           _INT, _INT, _P]
 lib.detfold_loopback_allreduce_dev.argtypes = [_P, _INT, _I64, _F, _P, _P]
 lib.detfold_all_gather.argtypes = [_P, _INT, _P, _I64, _P]
 lib.detfold_shard_plan.argtypes = [_I64, _INT, _P, _P]
@@ -79,6 +86,7 @@ for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
               "detfold_loopback_allreduce_staged_noalloc", "detfold_broadcast",
               "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
+              "detfold_one_shot_allreduce",
               "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
     getattr(lib, _name).restype = _INT
 
@@ -226,6 +234,28 @@ def status_loopback_allreduce_dev(table, W: int, length: int, mean_scale: float 
                                               _status_ptr(status), _stream(stream))
 
 
+def _raw_dev(x, nbytes: int, what: str) -> int:
+    """Address of a CUDA tensor of at least nbytes (any dtype), or an int."""
+    if isinstance(x, int):
+        return x
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous():
+        raise TypeError(f"{what}: expected a contiguous CUDA tensor")
+    if x.numel() * x.element_size() < nbytes:
+        raise ValueError(f"{what}: needs {nbytes} bytes, has {x.numel() * x.element_size()}")
+    return x.data_ptr()
+
+
+def status_one_shot_allreduce(arenas, W: int, length: int, mean_scale: float, link, epoch: int,
+                              stage, words, wait_ns: int = 1_000_000_000, drop_rank: int = -1,
+                              drop_at_exit: int = 0, stream=None) -> int:
+    tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
+    return lib.detfold_one_shot_allreduce(
+        tab, W, length, mean_scale, _raw_dev(link, DETFOLD_ONESHOT_LINK_BYTES, "link"), epoch,
+        _raw_dev(stage, W * length * 4, "stage"), _raw_dev(words, W * 4, "words"), wait_ns,
+        drop_rank, drop_at_exit, _stream(stream))
+
+
 # ------------------------------------------------------------------ raising calls (C names)
 
 def detfold_sum_stacked(out, stacked, W: int, length: int, stream=None) -> None:
@@ -284,6 +314,43 @@ def detfold_loopback_allreduce_dev(table, W: int, length: int, mean_scale: float
                                    status=None, stream=None) -> None:
     _check(status_loopback_allreduce_dev(table, W, length, mean_scale, status, stream),
            "detfold_loopback_allreduce_dev")
+
+
+def detfold_one_shot_allreduce(arenas, W: int, length: int, mean_scale: float, link, epoch: int,
+                               stage, words, wait_ns: int = 1_000_000_000, drop_rank: int = -1,
+                               drop_at_exit: int = 0, stream=None) -> None:
+    _check(status_one_shot_allreduce(arenas, W, length, mean_scale, link, epoch, stage, words,
+                                     wait_ns, drop_rank, drop_at_exit, stream),
+           "detfold_one_shot_allreduce")
+
+
+class OneShotLink:
+    """Device state of one emulated one-shot link between W ranks: barrier
+    flags (zero-filled once), W stage rows of up to max_len floats, the W
+    refusal words, and the host-side epoch, which grows by one per call."""
+
+    def __init__(self, W: int, max_len: int, device="cuda"):
+        import torch
+        self.W, self.max_len = W, max_len
+        self.link = torch.zeros(DETFOLD_ONESHOT_LINK_BYTES // 8, dtype=torch.int64, device=device)
+        self.stage = torch.empty(max(1, W * max_len), dtype=torch.float32, device=device)
+        self.words = torch.zeros(W, dtype=torch.int32, device=device)
+        self.epoch = 0
+
+    def all_reduce(self, arenas, mean_scale: float = 1.0, wait_ns: int = 1_000_000_000,
+                   drop_rank: int = -1, drop_at_exit: bool = False, stream=None) -> None:
+        n = arenas[0].numel()
+        if n > self.max_len or len(arenas) != self.W:
+            raise ValueError("arenas do not fit this link")
+        self.epoch += 1
+        self.words.zero_()
+        detfold_one_shot_allreduce(list(arenas), self.W, n, mean_scale, self.link, self.epoch,
+                                   self.stage, self.words, wait_ns, drop_rank,
+                                   1 if drop_at_exit else 0, stream)
+
+    def barrier_errors(self) -> list[int]:
+        """The refusal words of the last call: 0, 40043 (entry) or 40044 (exit)."""
+        return [int(x) for x in self.words.cpu()]
 
 
 def detfold_broadcast(dsts, ndst: int, src, length: int, stream=None) -> None:

@@ -10,6 +10,14 @@
 #include "detfold.h"
 #include "detfold_launch.cuh"
 
+namespace detfold {
+// One-shot all-reduce emulation, one cooperative launch (one_shot.cu).
+cudaError_t launch_one_shot(float *const *arenas, int W, int64_t len, float scale, int do_scale,
+                            void *link, unsigned long long epoch, float *stage, int *words,
+                            long long wait_ns, int drop_rank, int drop_at_exit,
+                            cudaStream_t stream);
+}  // namespace detfold
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -350,6 +358,30 @@ int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, f
     return cuda_status(detfold::launch_table((const float *const *)d_arenas, nullptr, d_status, W,
                                              len, mean_scale, do_scale, detfold::kAllReduce,
                                              (cudaStream_t)stream));
+}
+
+int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
+                               void *link, uint64_t epoch, float *stage, int *words,
+                               int64_t wait_ns, int drop_rank, int drop_at_exit, void *stream)
+{
+    if (!arenas || !link || !stage || !words) return DETFOLD_ERR_NULL;
+    if (W < 1 || W > DETFOLD_ONESHOT_MAX_W) return DETFOLD_ERR_WORLD;
+    if (len < 0 || len > DETFOLD_ONESHOT_MAX_LEN) return DETFOLD_ERR_LEN;
+    if (epoch < 1 || wait_ns < 1 || wait_ns > 2000000000LL || drop_rank < -1 || drop_rank >= W)
+        return DETFOLD_ERR_ARG;
+    if (((uintptr_t)link & 7u) || !aligned4(stage) || ((uintptr_t)words & 3u))
+        return DETFOLD_ERR_ALIGN;
+    if (int rc = arenas_valid(arenas, W, len)) return rc;
+    if (len == 0) return DETFOLD_OK;
+    const int64_t stage_bytes = (int64_t)W * len * 4;
+    for (int r = 0; r < W; ++r)
+        if (intersects(stage, stage_bytes, arenas[r], len * 4) ||
+            intersects(link, DETFOLD_ONESHOT_LINK_BYTES, arenas[r], len * 4))
+            return DETFOLD_ERR_OVERLAP;
+    if (intersects(stage, stage_bytes, link, DETFOLD_ONESHOT_LINK_BYTES)) return DETFOLD_ERR_OVERLAP;
+    return cuda_status(detfold::launch_one_shot(arenas, W, len, mean_scale, mean_scale != 1.0f ? 1 : 0,
+                                                link, epoch, stage, words, wait_ns, drop_rank,
+                                                drop_at_exit ? 1 : 0, (cudaStream_t)stream));
 }
 
 int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens)

@@ -161,6 +161,98 @@ __global__ void __launch_bounds__(256) fold_table_kernel(const __grid_constant__
         table_scalar_body<MODE>(p, s_src);
 }
 
+// Small payloads with W <= 8: every thread reads the (broadcast) table
+// entries into registers, checks them and picks the access width itself --
+// no shared memory and no block barrier between the table load and the data
+// loads, which is what the latency of a graph of small folds is made of.
+template <int WT, int VEC, int MODE>
+__device__ __forceinline__ void table_fixed_vec(const TableParams &p, const float *const (&src)[WT],
+                                                int64_t head)
+{
+    const int64_t nvec = (p.len - head) / VEC;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t v = gtid; v < nvec; v += stride) {
+        const int64_t e = head + v * VEC;
+        Vec<VEC> x[WT];
+#pragma unroll
+        for (int r = 0; r < WT; ++r) x[r] = ldv<VEC, false>(src[r] + e);
+        Vec<VEC> acc = x[0];
+#pragma unroll
+        for (int r = 1; r < WT; ++r)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc.v[j] = __fadd_rn(acc.v[j], x[r].v[j]);
+        if (p.do_scale) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc.v[j] = __fmul_rn(acc.v[j], p.scale);
+        }
+        if constexpr (MODE == kAllReduce) {
+#pragma unroll
+            for (int r = 0; r < WT; ++r) stv<VEC>(const_cast<float *>(src[r]) + e, acc);
+        } else {
+            stv<VEC>(p.out + e, acc);
+        }
+    }
+    const int64_t tail0 = head + nvec * VEC;
+    for (int part = 0; part < 2; ++part) {
+        const int64_t i = part == 0 ? gtid : tail0 + gtid;
+        if ((part == 0 && gtid < head) || (part == 1 && gtid < p.len - tail0)) {
+            float acc = ld1<false>(src[0] + i);
+#pragma unroll
+            for (int r = 1; r < WT; ++r) acc = __fadd_rn(acc, ld1<false>(src[r] + i));
+            if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+            if constexpr (MODE == kAllReduce) {
+#pragma unroll
+                for (int r = 0; r < WT; ++r) st1(const_cast<float *>(src[r]) + i, acc);
+            } else {
+                st1(p.out + i, acc);
+            }
+        }
+    }
+}
+
+template <int WT, int MODE>
+__global__ void __launch_bounds__(256) fold_table_fixed_kernel(const __grid_constant__ TableParams p)
+{
+    pdl_enter(p.pdl);
+    const float *src[WT];
+#pragma unroll
+    for (int r = 0; r < WT; ++r) src[r] = p.table[r];
+    int code = DETFOLD_OK;
+#pragma unroll
+    for (int r = 0; r < WT; ++r) {
+        if (code == DETFOLD_OK && src[r] == nullptr) code = DETFOLD_ERR_NULL;
+        if (code == DETFOLD_OK && ((uintptr_t)src[r] & 3u)) code = DETFOLD_ERR_ALIGN;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = code;
+    if (code != DETFOLD_OK) return;
+    bool same8 = (MODE == kAllReduce) || phase_of(p.out, 8) == phase_of(src[0], 8);
+    bool same4 = (MODE == kAllReduce) || phase_of(p.out, 4) == phase_of(src[0], 4);
+#pragma unroll
+    for (int r = 1; r < WT; ++r) {
+        same8 = same8 && phase_of(src[r], 8) == phase_of(src[0], 8);
+        same4 = same4 && phase_of(src[r], 4) == phase_of(src[0], 4);
+    }
+    if (same8) {
+        int64_t head = (8 - phase_of(src[0], 8)) % 8;
+        table_fixed_vec<WT, 8, MODE>(p, src, head > p.len ? p.len : head);
+    } else if (same4) {
+        int64_t head = (4 - phase_of(src[0], 4)) % 4;
+        table_fixed_vec<WT, 4, MODE>(p, src, head > p.len ? p.len : head);
+    } else {
+        table_scalar_body<MODE>(p, src);
+    }
+}
+
+template <int WT>
+cudaError_t launch_table_fixed(const TableParams &p, int64_t work, bool small, int mode,
+                               cudaStream_t stream)
+{
+    if (mode == kAllReduce)
+        return launch_kernel<fold_table_fixed_kernel<WT, kAllReduce>>(p, work, 1, small, 256, 0, stream);
+    return launch_kernel<fold_table_fixed_kernel<WT, kSumCoherent>>(p, work, 1, small, 256, 0, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
@@ -177,6 +269,19 @@ cudaError_t launch_table(const float *const *d_table, float *out, int *d_status,
     const bool small = len <= DETFOLD_SMALL_LEN;
     p.pdl = (small && DETFOLD_SMALL_PDL) ? 1 : 0;
     const int64_t work = (len + 7) / 8 > 0 ? (len + 7) / 8 : 1;  // vectors if 32-byte access
+    // Small payloads: the register-table kernel (shortest dependent chain).
+    // Bandwidth-sized calls: the shared-memory table kernel (fewer registers).
+    switch (small ? W : 0) {
+    case 1: return launch_table_fixed<1>(p, work, small, mode, stream);
+    case 2: return launch_table_fixed<2>(p, work, small, mode, stream);
+    case 3: return launch_table_fixed<3>(p, work, small, mode, stream);
+    case 4: return launch_table_fixed<4>(p, work, small, mode, stream);
+    case 5: return launch_table_fixed<5>(p, work, small, mode, stream);
+    case 6: return launch_table_fixed<6>(p, work, small, mode, stream);
+    case 7: return launch_table_fixed<7>(p, work, small, mode, stream);
+    case 8: return launch_table_fixed<8>(p, work, small, mode, stream);
+    default: break;
+    }
     if (mode == kAllReduce)
         return launch_kernel<fold_table_kernel<kAllReduce>>(p, work, 1, small, 256, 0, stream);
     return launch_kernel<fold_table_kernel<kSumCoherent>>(p, work, 1, small, 256, 0, stream);

@@ -174,6 +174,46 @@ int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, f
                                    int *d_status, void *stream);
 
 /*
+ * One-shot all-reduce, emulated on one device in a single cooperative launch
+ * (memra-engine 0.128.0 tests/tp_ar_gpu.rs,
+ * `one_shot_all_reduce_matches_the_host_sum_bitwise`). Each rank is a group of
+ * CTAs. An entry barrier and an exit barrier made of per-CTA epoch flags
+ * frame the fold: every rank folds all W arenas in ascending rank order into
+ * its stage row, times mean_scale (skipped when exactly 1.0f), and after the
+ * exit barrier copies the row into its own arena. End state and bits are
+ * those of detfold_loopback_allreduce.
+ *   arenas    host array of W <= DETFOLD_ONESHOT_MAX_W device pointers to len
+ *             f32, pairwise disjoint.
+ *   len       <= DETFOLD_ONESHOT_MAX_LEN (a small-payload primitive).
+ *   link      device, DETFOLD_ONESHOT_LINK_BYTES, 8-byte aligned, zero-filled
+ *             once before the first call on it, then reused unchanged.
+ *   epoch     >= 1 and larger than every epoch used before on this link (the
+ *             barrier flags only grow, so nothing needs resetting after a
+ *             refused call).
+ *   stage     device, W * len f32 scratch, disjoint from the arenas.
+ *   words     device, W ints: rank r's refusal word -- DETFOLD_OK, or
+ *             DETFOLD_ONESHOT_REFUSE_ENTRY / _EXIT when its bounded wait at
+ *             that barrier ran out, in which case its arena is untouched.
+ *             Read the words before the numbers.
+ *   wait_ns   bound on each barrier wait, 1 .. 2e9 ns (DETFOLD_ERR_ARG else).
+ *   drop_rank -1, or a rank that leaves without publishing at one barrier
+ *             (the entry barrier, or the exit barrier when drop_at_exit != 0)
+ *             so that the others' waits run out: failure detection is tested
+ *             this way, with no fault and no hang.
+ * DETFOLD_ERR_CUDA with cudaErrorCooperativeLaunchTooLarge when W rank
+ * groups cannot be co-resident.
+ */
+#define DETFOLD_ONESHOT_MAX_W 64
+#define DETFOLD_ONESHOT_MAX_LEN ((int64_t)1 << 22)
+#define DETFOLD_ONESHOT_MAX_CTAS 1024
+#define DETFOLD_ONESHOT_LINK_BYTES (2 * DETFOLD_ONESHOT_MAX_CTAS * 8)
+#define DETFOLD_ONESHOT_REFUSE_ENTRY 40043
+#define DETFOLD_ONESHOT_REFUSE_EXIT 40044
+int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
+                               void *link, uint64_t epoch, float *stage, int *words,
+                               int64_t wait_ns, int drop_rank, int drop_at_exit, void *stream);
+
+/*
  * Broadcast, pure byte movement (memra-engine 0.128.0 tests/tp_ar_gpu.rs,
  * `broadcast_and_all_gather_move_bytes_exactly`: rank 0's buffer lands on
  * every other rank byte for byte): dsts[k][i] = src[i] for every k.

@@ -212,6 +212,33 @@ def test_validation_device_tables(df):
 
 
 @no_gpu_only
+def test_validation_one_shot(df):
+    L, S = df.lib, df.STATUS
+    arenas = _tab(A, A + 4096)
+    link, stage, words = A + (1 << 20), A + (1 << 21), A + (1 << 22)
+    ok = dict(link=link, epoch=1, stage=stage, words=words, wait=1000000, drop=-1, at_exit=0)
+
+    def call(arenas=arenas, W=2, n=64, **kw):
+        a = {**ok, **kw}
+        return L.detfold_one_shot_allreduce(arenas, W, n, 1.0, a["link"], a["epoch"], a["stage"],
+                                            a["words"], a["wait"], a["drop"], a["at_exit"], None)
+    assert call(link=None) == S["DETFOLD_ERR_NULL"]
+    assert call(stage=None) == S["DETFOLD_ERR_NULL"]
+    assert call(words=None) == S["DETFOLD_ERR_NULL"]
+    assert call(W=0) == S["DETFOLD_ERR_WORLD"]
+    assert call(W=65) == S["DETFOLD_ERR_WORLD"]
+    assert call(n=(1 << 22) + 1) == S["DETFOLD_ERR_LEN"]
+    assert call(epoch=0) == S["DETFOLD_ERR_ARG"]
+    assert call(wait=0) == S["DETFOLD_ERR_ARG"]
+    assert call(wait=3_000_000_000) == S["DETFOLD_ERR_ARG"]
+    assert call(drop=2) == S["DETFOLD_ERR_ARG"]
+    assert call(link=link + 4) == S["DETFOLD_ERR_ALIGN"]
+    assert call(arenas=_tab(A, A + 8)) == S["DETFOLD_ERR_OVERLAP"]
+    assert call(stage=A + 100) == S["DETFOLD_ERR_OVERLAP"]
+    assert call(n=0) == S["DETFOLD_OK"]
+
+
+@no_gpu_only
 def test_validation_scale_and_floor(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_scale(None, 8, 0.5, None) == S["DETFOLD_ERR_NULL"]

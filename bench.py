@@ -424,6 +424,12 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
     out["one_shot_barrier_errors"] = link.barrier_errors()
     out["fused_W2_16KiB_us_per_call_same_timing"] = round(
         per_call_us(lambda: df.detfold_loopback_allreduce(arenas, 2, n, 1.0)), 2)
+    # mismatched phases at the C3 size: the rows of an [8][2^26 - 3] stack sit
+    # at eight different 4-byte phases, so the realigned kernel runs
+    nm = C3_N - 3
+    ms = t(lambda: df.detfold_sum_stacked(wl.c3_out2, wl.c3, C3_W, nm))
+    out["stacked_mismatched_W8_2^26-3"] = {"ms": round(ms, 4),
+                                           "gbs": round((C3_W + 1) * nm * 4 / (ms * 1e-3) / 1e9, 1)}
     table = df.device_table(wl.c3_rows)
     ms = t(lambda: df.detfold_sum_ptrs_dev(wl.c3_out2, table, C3_W, C3_N))
     out["sum_ptrs_dev_W8_2^26"] = {"ms": round(ms, 4),

@@ -400,4 +400,135 @@ __global__ void __launch_bounds__(max_threads<MODE>()) fold_scalar_generic_kerne
     }
 }
 
+// ---------------------------------------------------------------- realigned vector kernel
+
+// Sum modes with sources at different 4-byte phases (e.g. the rows of a
+// [W][len] stack when len % 8 != 0). Vectors follow the output's 32-byte
+// alignment; source r's eight elements of output vector v straddle two
+// aligned 32-byte vectors, at element shift d_r = phase of (src_r + head).
+// Each lane loads one aligned vector per source; the upper half of its
+// straddle is the next lane's vector, taken with a warp shuffle. A warp
+// therefore produces 31 output vectors per pass: lane 31 only loads, to feed
+// lane 30. The body covers output vectors 1 .. nvec-2 (loads 1 .. nvec-1),
+// which keeps every load inside every source; the edges are scalar.
+template <int NT>
+struct RealignParams {
+    const float *src[NT];
+    int shift[NT];  // d_r in 0..7
+    float *out;
+    int64_t len, head, nvec;
+    float scale;
+    int do_scale;
+    int pdl;
+};
+
+template <bool NC>
+__device__ __forceinline__ Vec<8> ldv8_l1(const float *p)
+{
+    Vec<8> r;
+    if constexpr (NC)
+        asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
+                       "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
+                       "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+                     : "l"(p));
+    return r;
+}
+
+template <int D>
+__device__ __forceinline__ Vec<8> take8(const Vec<8> &a, const Vec<8> &b)
+{
+    Vec<8> x;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x.v[k] = (k + D < 8) ? a.v[k + D] : b.v[k + D - 8];
+    return x;
+}
+
+template <int W, int MODE>
+__global__ void __launch_bounds__(256) fold_realign_kernel(const __grid_constant__ RealignParams<W> p)
+{
+    static_assert(MODE != kAllReduce, "all-reduce stores need every arena aligned");
+    constexpr bool NC = (MODE == kSumNC);
+    pdl_enter(p.pdl);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = stride >> 5;
+    // warp-uniform loop: every lane of a warp runs every pass (for the shuffles)
+    for (int64_t c = gtid >> 5; 1 + c * 31 < p.nvec - 1; c += nwarps) {
+        const int64_t v = 1 + c * 31 + lane;
+        const bool loads = v <= p.nvec - 1;
+        const bool writes = lane < 31 && v <= p.nvec - 2;
+        const int64_t e = p.head + v * 8;
+        Vec<8> lo[W];
+#pragma unroll
+        for (int r = 0; r < W; ++r) {
+            if (loads) {
+                lo[r] = ldv8_l1<NC>(p.src[r] + e - p.shift[r]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) lo[r].v[k] = 0.0f;
+            }
+        }
+        Vec<8> acc;
+#pragma unroll
+        for (int r = 0; r < W; ++r) {
+            Vec<8> x;
+            const int d = p.shift[r];  // uniform: no divergence
+            if (d == 0) {
+                x = lo[r];
+            } else {
+                Vec<8> hi;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) hi.v[k] = __shfl_down_sync(0xffffffffu, lo[r].v[k], 1);
+                switch (d) {
+                case 1: x = take8<1>(lo[r], hi); break;
+                case 2: x = take8<2>(lo[r], hi); break;
+                case 3: x = take8<3>(lo[r], hi); break;
+                case 4: x = take8<4>(lo[r], hi); break;
+                case 5: x = take8<5>(lo[r], hi); break;
+                case 6: x = take8<6>(lo[r], hi); break;
+                default: x = take8<7>(lo[r], hi); break;
+                }
+            }
+            if (r == 0) {
+                acc = x;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc.v[k] = __fadd_rn(acc.v[k], x.v[k]);
+            }
+        }
+        if (writes) {
+            if (p.do_scale) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc.v[k] = __fmul_rn(acc.v[k], p.scale);
+            }
+            stv<8>(p.out + e, acc);
+        }
+    }
+    // scalar edges: [0, lo_end) and [hi_begin, len), disjoint from the body
+    // and from each other
+    const int64_t body = p.nvec >= 3 ? p.nvec - 2 : 0;
+    const int64_t lo_end = body ? p.head + 8 : p.len;
+    const int64_t hi_begin = body ? p.head + 8 * (p.nvec - 1) : p.len;
+    for (int64_t i = gtid; i < lo_end; i += stride) {
+        float acc = ld1<NC>(p.src[0] + i);
+#pragma unroll
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
+        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+        st1(p.out + i, acc);
+    }
+    for (int64_t i = hi_begin + gtid; i < p.len; i += stride) {
+        float acc = ld1<NC>(p.src[0] + i);
+#pragma unroll
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
+        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+        st1(p.out + i, acc);
+    }
+}
+
 }  // namespace detfold

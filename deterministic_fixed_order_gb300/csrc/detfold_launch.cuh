@@ -157,8 +157,29 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         constexpr int U = u_for<MODE>(W, 4);
         return launch_kernel<fold_vec_kernel<W, 4, U, MODE>>(p, pl.nvec, U, small, T, C, stream);
     }
-    constexpr int U = u_for<MODE>(W, 0);
-    return launch_kernel<fold_scalar_kernel<W, U, MODE>>(p, s.len, U, small, T, C, stream);
+    if constexpr (MODE != kAllReduce) {
+        // no common phase: realign every source onto the output's 32-byte grid
+        RealignParams<W> q = {};
+        const int ph = elem_phase(s.out, 8);
+        q.head = (8 - ph) % 8;
+        if (q.head > s.len) q.head = s.len;
+        q.nvec = (s.len - q.head) / 8;
+        for (int r = 0; r < W; ++r) {
+            q.src[r] = s.src[r];
+            q.shift[r] = elem_phase(s.src[r] + q.head, 8);
+        }
+        q.out = s.out;
+        q.len = s.len;
+        q.scale = s.scale;
+        q.do_scale = s.do_scale;
+        q.pdl = p.pdl;
+        // a warp covers 31 vectors per pass
+        const int64_t work = q.nvec > 2 ? (q.nvec - 2 + 30) / 31 * 32 : 32;
+        return launch_kernel<fold_realign_kernel<W, MODE>>(q, work, 1, small, 256, 0, stream);
+    } else {
+        constexpr int U = u_for<MODE>(W, 0);
+        return launch_kernel<fold_scalar_kernel<W, U, MODE>>(p, s.len, U, small, T, C, stream);
+    }
 }
 
 template <int MODE>

@@ -59,18 +59,17 @@ GRAPH_NODES = 10_000
 # DRAM traffic of the dominant kernel from one ncu capture, keyed by a hash of
 # the kernel sources it was taken on; null once the kernel has changed.
 NCU_TRAFFIC = {
-    # profiles/fold_vec_kernel_W8_stacked.md: full-size C3 launch (8 x 2^26),
+    # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_vec_kernel<W=8,kSumNC>": {"bytes_per_launch": 2150019072 + 261127424,
-                                    "kernel_hash": "60ca0eb98dfe56ad"},
-    # profiles/fold_vec_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_vec_kernel<W=4,kAllReduce>": {"bytes_per_launch": 1600070144 + 1538395904,
-                                        "kernel_hash": "60ca0eb98dfe56ad"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147698688 + 258952448,
+                                  "kernel_hash": "ed371981487c166c"},
+    # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600028160 + 1538253568,
+                                         "kernel_hash": "ed371981487c166c"},
 }
 
-
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "fold_sum_nc.cu",
-                "fold_sum_coherent.cu", "fold_allreduce.cu")
+                "fold_sum_coherent.cu", "fold_allreduce.cu", "fold_bulk.cu")
 
 
 def kernel_source_hash() -> str:
@@ -585,10 +584,10 @@ def run_gpu(args) -> None:
     c3_ms = (per_row["c3_stacked"]["ms"] + per_row["c3_ptrs"]["ms"]) / 2
     c4_ms = per_row["c4_fused"]["ms"]
     if 2 * c3_ms >= c4_ms:
-        dom, dom_bytes, dom_ms = ("fold_vec_kernel<W=8,kSumNC> (c3_stacked+c3_ptrs)",
+        dom, dom_bytes, dom_ms = ("fold_bulk_kernel<W=8,sum> (c3_stacked+c3_ptrs)",
                                   bytes_by_row["c3_stacked"], c3_ms)
     else:
-        dom, dom_bytes, dom_ms = ("fold_vec_kernel<W=4,kAllReduce> (c4_fused)",
+        dom, dom_bytes, dom_ms = ("fold_bulk_kernel<W=4,all-reduce> (c4_fused)",
                                   bytes_by_row["c4_fused"], c4_ms)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     khash = kernel_source_hash()

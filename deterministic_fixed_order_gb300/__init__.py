@@ -82,12 +82,14 @@ lib.detfold_status_string.argtypes = [_INT]
 lib.detfold_status_string.restype = ctypes.c_char_p
 lib.detfold_last_cuda_error.argtypes = []
 lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
+lib.detfold_pipeline_timeouts.argtypes = [_P]
 for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
               "detfold_loopback_allreduce_staged_noalloc", "detfold_broadcast",
               "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
               "detfold_one_shot_allreduce",
-              "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor"):
+              "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor",
+              "detfold_pipeline_timeouts"):
     getattr(lib, _name).restype = _INT
 
 
@@ -374,6 +376,14 @@ def detfold_status_string(status: int) -> str:
 
 def detfold_last_cuda_error() -> int:
     return lib.detfold_last_cuda_error()
+
+
+def detfold_pipeline_timeouts() -> int:
+    """Bounded waits that ran out in the bulk-async path (should be 0).
+    Synchronizes the device."""
+    c = ctypes.c_int64(0)
+    _check(lib.detfold_pipeline_timeouts(ctypes.byref(c)), "detfold_pipeline_timeouts")
+    return c.value
 
 
 def detfold_launch_floor(count: int, pdl: int = 1, stream=None) -> None:

@@ -413,6 +413,15 @@ const char *detfold_status_string(int status)
 
 int detfold_last_cuda_error(void) { return g_last_cuda_error; }
 
+int detfold_pipeline_timeouts(int64_t *count)
+{
+    if (!count) return DETFOLD_ERR_NULL;
+    unsigned long long c = 0;
+    if (int rc = cuda_status(detfold::read_pipeline_timeouts(&c))) return rc;
+    *count = (int64_t)c;
+    return DETFOLD_OK;
+}
+
 int detfold_launch_floor(int count, int pdl, void *stream)
 {
     if (count < 0) return DETFOLD_ERR_ARG;

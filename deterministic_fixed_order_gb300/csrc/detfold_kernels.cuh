@@ -64,6 +64,12 @@
 #ifndef DETFOLD_AR_THREADS
 #define DETFOLD_AR_THREADS 256  // CTA size of the bandwidth path, all-reduce mode
 #endif
+#ifndef DETFOLD_USE_BULK
+#define DETFOLD_USE_BULK 1  // bulk-async (TMA) staged path for large aligned calls
+#endif
+#ifndef DETFOLD_BULK_MIN_LEN
+#define DETFOLD_BULK_MIN_LEN (1 << 20)  // elements at or above: the bulk path
+#endif
 #ifndef DETFOLD_SMALL_PDL
 #define DETFOLD_SMALL_PDL 1  // programmatic dependent launch on the small path
 #endif

@@ -141,11 +141,19 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
     return p;
 }
 
+// Bulk-async (TMA) staged bandwidth path (fold_bulk.cu).
+int bulk_tile_floats(int W);
+cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream);
+cudaError_t read_pipeline_timeouts(unsigned long long *count);
+
 template <int W, int MODE>
 inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
 {
     const Plan pl = make_plan(s);
     const bool small = s.len <= DETFOLD_SMALL_LEN;
+    if (DETFOLD_USE_BULK && !small && pl.vec >= 4 && s.len >= DETFOLD_BULK_MIN_LEN &&
+        s.len - pl.head >= bulk_tile_floats(W))
+        return launch_bulk(s, pl.head, stream);
     const FoldParams<W> p = fill_params<W>(s, pl, small);
     constexpr int T = bw_threads<MODE>();
     constexpr int C = ctas_per_sm_cap<MODE>();

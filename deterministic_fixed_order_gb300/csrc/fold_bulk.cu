@@ -1,0 +1,344 @@
+// Bandwidth path with bulk-async (TMA) staging: the fold and the fused
+// all-reduce for large aligned calls.
+//
+// Per CTA, one producer lane streams tiles of every rank's operand into a
+// ring of shared-memory stages with cp.async.bulk (global -> shared,
+// completion on an mbarrier with a byte count); consumer warps fold the
+// stage in ascending rank order with __fadd_rn (the same per-element chain
+// as every other fold here, so the same bits: mamba-rs 0.6.2
+// src/dist/reducer.rs, `reduce_sum_reference`), apply the mean multiply,
+// write the result tile to shared memory, and one consumer thread bulk-stores
+// it (shared -> global) to the output -- or to all W arenas for the
+// all-reduce, so the result is read from shared memory W times instead of
+// being recomputed or reloaded. DRAM sees long contiguous requests (one tile
+// per rank and stage) and the SMs issue a handful of instructions per tile.
+//
+// Every mbarrier wait is bounded (%globaltimer, about one second, and a poll
+// cap). On expiry the kernel counts the event in a device counter that
+// detfold_pipeline_timeouts() reads, waits (bounded) for its own copies in
+// flight, and stops; the call's output is then incomplete and the counter
+// says so.
+//
+// Preconditions, checked by the dispatcher: W <= 8, every operand at the same
+// 32-byte phase (tiles then start 32-byte aligned), at least one whole tile.
+// The head before the first tile and the tail after the last are folded by
+// scalar code in the same launch.
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "detfold.h"
+#include "detfold_launch.cuh"
+
+namespace detfold {
+
+namespace {
+
+__device__ unsigned long long g_pipeline_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ long long now_ns()
+{
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.
+__device__ bool mbar_wait(uint64_t *b, uint32_t parity)
+{
+    const long long t0 = now_ns();
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try(b, parity)) return true;
+        if (now_ns() - t0 > 1000000000LL) break;
+    }
+    atomicAdd(&g_pipeline_timeouts, 1ull);
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void named_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Tile shapes from GB300 sweeps: 8 KB per rank and 3 stages up to W = 4,
+// 4 KB per rank and 2 stages above; four consumer warps.
+#ifndef DETFOLD_BULK_T_LO
+#define DETFOLD_BULK_T_LO 2048  // floats per rank per tile, W <= 4
+#endif
+#ifndef DETFOLD_BULK_S_LO
+#define DETFOLD_BULK_S_LO 3     // stages, W <= 4
+#endif
+#ifndef DETFOLD_BULK_T_HI
+#define DETFOLD_BULK_T_HI 1024  // floats per rank per tile, W > 4
+#endif
+#ifndef DETFOLD_BULK_S_HI
+#define DETFOLD_BULK_S_HI 2     // stages, W > 4
+#endif
+#ifndef DETFOLD_BULK_NCW
+#define DETFOLD_BULK_NCW 4      // consumer warps
+#endif
+#ifndef DETFOLD_BULK_CTAS_PER_SM
+#define DETFOLD_BULK_CTAS_PER_SM 2  // 0: as many as shared memory allows
+#endif
+template <int W>
+struct BulkShape {
+    static constexpr int T = W <= 4 ? DETFOLD_BULK_T_LO : DETFOLD_BULK_T_HI;
+    static constexpr int S = W <= 4 ? DETFOLD_BULK_S_LO : DETFOLD_BULK_S_HI;
+    static constexpr int NCW = DETFOLD_BULK_NCW;
+    static constexpr int THREADS = 32 * (1 + NCW);
+    static constexpr size_t SMEM = (size_t)S * (W + 1) * T * 4 + 2 * S * 8;
+};
+
+template <int W>
+struct BulkParams {
+    float *a[W];   // sources (all-reduce: also the destinations)
+    float *out;    // sum destination
+    int64_t len, head, ntiles;
+    float scale;
+    int do_scale;
+};
+
+template <int W, int MODE>
+__global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const __grid_constant__ BulkParams<W> p)
+{
+    using Sh = BulkShape<W>;
+    constexpr int T = Sh::T, S = Sh::S, NC = 32 * Sh::NCW;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float *in = (float *)smem;                       // [S][W][T]
+    float *res = in + (size_t)S * W * T;             // [S][T]
+    uint64_t *full = (uint64_t *)(res + (size_t)S * T);
+    uint64_t *empty = full + S;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (threadIdx.x < 32) {  // producer warp: one lane issues the loads
+        if (threadIdx.x == 0) {
+            long long k = 0;
+            for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
+                const int s = (int)(k % S);
+                if (k >= S && !mbar_wait(&empty[s], (uint32_t)(((k / S) - 1) & 1))) break;
+                mbar_arrive_expect(&full[s], W * T * 4);
+#pragma unroll
+                for (int r = 0; r < W; ++r)
+                    bulk_load(in + ((size_t)s * W + r) * T, p.a[r] + p.head + t * T, T * 4, &full[s]);
+            }
+            // before this CTA may exit, every load it issued has landed
+            for (long long j = (k > S ? k - S : 0); j < k; ++j)
+                if (!mbar_wait(&full[j % S], (uint32_t)((j / S) & 1))) break;
+        }
+        return;
+    }
+
+    const int tc = threadIdx.x - 32;
+    long long k = 0;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
+        const int s = (int)(k % S);
+        if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) break;
+        if (tc == 0) bulk_wait_read<S - 1>();  // the store of tile k-S has read res[s]
+        named_sync(1, NC);
+        const float *src = in + (size_t)s * W * T;
+        float *dst = res + (size_t)s * T;
+        for (int j = tc * 4; j < T; j += NC * 4) {
+            float4 acc = *(const float4 *)(src + j);
+#pragma unroll
+            for (int r = 1; r < W; ++r) {
+                const float4 x = *(const float4 *)(src + (size_t)r * T + j);
+                acc.x = __fadd_rn(acc.x, x.x);
+                acc.y = __fadd_rn(acc.y, x.y);
+                acc.z = __fadd_rn(acc.z, x.z);
+                acc.w = __fadd_rn(acc.w, x.w);
+            }
+            if (p.do_scale) {
+                acc.x = __fmul_rn(acc.x, p.scale);
+                acc.y = __fmul_rn(acc.y, p.scale);
+                acc.z = __fmul_rn(acc.z, p.scale);
+                acc.w = __fmul_rn(acc.w, p.scale);
+            }
+            *(float4 *)(dst + j) = acc;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk store
+        named_sync(1, NC);
+        if (tc == 0) {
+            mbar_arrive(&empty[s]);  // the input stage may be refilled
+            const int64_t e = p.head + t * T;
+            if constexpr (MODE == kAllReduce) {
+#pragma unroll
+                for (int r = 0; r < W; ++r) bulk_store(p.a[r] + e, dst, T * 4);
+            } else {
+                bulk_store(p.out + e, dst, T * 4);
+            }
+            bulk_commit();
+        }
+    }
+    if (tc == 0) bulk_wait_all();
+
+    // head [0, head) and tail [head + ntiles*T, len): scalar, by the last CTA
+    if (blockIdx.x == gridDim.x - 1) {
+        const int64_t tail0 = p.head + p.ntiles * T;
+        const int64_t nhead = p.head, ntail = p.len - tail0;
+        for (int64_t q = tc; q < nhead + ntail; q += NC) {
+            const int64_t i = q < nhead ? q : tail0 + (q - nhead);
+            float acc = ld1<false>(p.a[0] + i);
+#pragma unroll
+            for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<false>(p.a[r] + i));
+            if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+            if constexpr (MODE == kAllReduce) {
+#pragma unroll
+                for (int r = 0; r < W; ++r) st1(p.a[r] + i, acc);
+            } else {
+                st1(p.out + i, acc);
+            }
+        }
+    }
+}
+
+// Shared-memory opt-in and resident CTAs, once per kernel and device.
+template <int W, int MODE>
+cudaError_t bulk_grid(int *grid)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        using Sh = BulkShape<W>;
+        e = cudaFuncSetAttribute(fold_bulk_kernel<W, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fold_bulk_kernel<W, MODE>, Sh::THREADS,
+                                                          Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        if (DETFOLD_BULK_CTAS_PER_SM > 0 && per_sm > DETFOLD_BULK_CTAS_PER_SM) per_sm = DETFOLD_BULK_CTAS_PER_SM;
+        v = sms * (per_sm > 0 ? per_sm : 1);
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    *grid = v;
+    return cudaSuccess;
+}
+
+template <int W, int MODE>
+cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t stream)
+{
+    using Sh = BulkShape<W>;
+    BulkParams<W> p = {};
+    for (int r = 0; r < W; ++r) p.a[r] = const_cast<float *>(s.src[r]);
+    p.out = s.out;
+    p.len = s.len;
+    p.head = head;
+    p.ntiles = (s.len - head) / Sh::T;
+    p.scale = s.scale;
+    p.do_scale = s.do_scale;
+    int cap = 0;
+    cudaError_t e = bulk_grid<W, MODE>(&cap);
+    if (e != cudaSuccess) return e;
+    int64_t grid = p.ntiles < cap ? p.ntiles : cap;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(Sh::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, fold_bulk_kernel<W, MODE>, p);
+}
+
+template <int MODE>
+cudaError_t launch_bulk_mode(const LaunchSpec &s, int64_t head, cudaStream_t stream)
+{
+    switch (s.W) {
+    case 1: return launch_bulk_fixed<1, MODE>(s, head, stream);
+    case 2: return launch_bulk_fixed<2, MODE>(s, head, stream);
+    case 3: return launch_bulk_fixed<3, MODE>(s, head, stream);
+    case 4: return launch_bulk_fixed<4, MODE>(s, head, stream);
+    case 5: return launch_bulk_fixed<5, MODE>(s, head, stream);
+    case 6: return launch_bulk_fixed<6, MODE>(s, head, stream);
+    case 7: return launch_bulk_fixed<7, MODE>(s, head, stream);
+    default: return launch_bulk_fixed<8, MODE>(s, head, stream);
+    }
+}
+
+}  // namespace
+
+int bulk_tile_floats(int W) { return W <= 4 ? BulkShape<4>::T : BulkShape<8>::T; }
+
+cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream)
+{
+    if (s.mode == kAllReduce) return launch_bulk_mode<kAllReduce>(s, head, stream);
+    return launch_bulk_mode<kSumCoherent>(s, head, stream);
+}
+
+cudaError_t read_pipeline_timeouts(unsigned long long *count)
+{
+    return cudaMemcpyFromSymbol(count, g_pipeline_timeouts, sizeof(*count));
+}
+
+}  // namespace detfold

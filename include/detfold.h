@@ -284,6 +284,17 @@ const char *detfold_status_string(int status);
 int detfold_last_cuda_error(void);
 
 /*
+ * Number of bounded waits that ran out, since the library was loaded, in the
+ * bulk-async (TMA) staged bandwidth path that large aligned folds and
+ * all-reduces use (W <= 8, len >= 2^20). Each such wait stops its CTA early,
+ * so any nonzero count means some output is incomplete. It should always be
+ * 0; tests check that. Synchronous: it reads a device counter (implicitly
+ * synchronizing the device), so it is a diagnostic, not for hot loops.
+ *   count  host, written.
+ */
+int detfold_pipeline_timeouts(int64_t *count);
+
+/*
  * Launch-latency floor probe: enqueues `count` launches of an empty kernel
  * (one CTA of 32 threads) on `stream`, with programmatic dependent launch
  * when pdl != 0, exactly as the small-payload fold path launches. Used to

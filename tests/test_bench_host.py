@@ -1,0 +1,50 @@
+"""Host-side pieces of bench.py, checked without a GPU: the byte accounting
+of every row, the peak lookup, the kernel-source hash and the reference arm."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_row_bytes_follow_the_algorithmic_formulas():
+    b = bench.row_bytes()
+    assert b["c3_stacked"] == 9 * (1 << 26) * 4 == 2_415_919_104
+    assert b["c4_fused"] == b["c4_staged"] == 2 * 4 * 100_000_000 * 4
+    n5 = (1 << 20) + 7
+    assert b["c5_w3"] == (4 + 2 + 6) * n5 * 4
+    assert b["c5_w6"] == (7 + 2 + 12) * n5 * 4
+    assert b["c2_4096"] == 3 * 4096 * 4
+
+
+def test_kernel_hash_covers_existing_files_and_is_stable():
+    h1, h2 = bench.kernel_source_hash(), bench.kernel_source_hash()
+    assert h1 == h2 and len(h1) == 16
+    for f in bench.KERNEL_FILES:
+        assert os.path.exists(os.path.join(ROOT, "deterministic_fixed_order_gb300", "csrc", f))
+
+
+def test_peak_lookup_has_a_named_source():
+    peak, src = bench.peaks()
+    assert peak > 1000 and src in ("measured", "fallback")
+
+
+def test_whole_job_value():
+    assert abs(bench.whole_job_gbs(2, 10_000_000_000, 2.0) - 10_000.0) < 1e-9
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "cpu_baseline", "e2e", "impl"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["e2e"]["h2d_bytes_per_step"] == 0

@@ -404,3 +404,56 @@ def test_c4_full_size_w4_fused_and_staged_bitwise():
         for r in range(W):
             assert_bitwise(staged[r].cpu().numpy(), exp[r], f"C4 staged flags={flags} rank {r}")
         del staged
+
+
+# ------------------------------------------------------------------ degenerate and extreme inputs
+
+def _nonfinite_rows(W, n, seed):
+    rows = gen.normal_rows(W, n)
+    rng = np.random.default_rng(seed)
+    specials = np.array([np.inf, -np.inf, np.nan], dtype=np.float32)
+    for r in range(W):
+        pick = rng.random(n) < 0.02
+        rows[r, pick] = specials[rng.integers(0, 3, size=int(pick.sum()))]
+    return rows
+
+
+@pytest.mark.parametrize("W", [2, 3, 8])
+@pytest.mark.parametrize("n", [4099, (1 << 20) + 7])
+def test_nonfinite_inputs_match_by_class(W, n):
+    # Inf and NaN propagate through the chain on both sides. Finite and
+    # infinite results must match bitwise; NaN results must be NaN on both
+    # sides (a GPU returns a canonical NaN, a host may keep an input payload).
+    rows = _nonfinite_rows(W, n, 17 + W)
+    want = oracle.fold(rows)
+    for got in (run_stacked(rows), run_ptrs(rows), run_allreduce(rows)[W - 1]):
+        nan_w, nan_g = np.isnan(want), np.isnan(got)
+        assert np.array_equal(nan_w, nan_g), "NaN positions differ"
+        assert_bitwise(got[~nan_g], want[~nan_w], f"non-NaN words W={W} n={n}")
+        assert nan_w.sum() > 0 and np.isinf(want).sum() > 0
+
+
+@pytest.mark.slow
+def test_lengths_beyond_int32():
+    # 64-bit element indexing: the reference's kernel ABI stops at i32 lengths.
+    n = (1 << 31) + 77
+    rows = gen.c1_rows(2, n)                       # 17.2 GB of host data
+    d = torch.from_numpy(rows).cuda()
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    df.detfold_sum_stacked(out, d, 2, n)
+    torch.cuda.synchronize()
+    idx = np.unique(np.r_[np.arange(0, 64), np.arange((1 << 31) - 64, (1 << 31) + 64),
+                          np.arange(n - 64, n),
+                          np.random.default_rng(5).integers(0, n, 4096)])
+    want = oracle.fold(np.ascontiguousarray(rows[:, idx]))
+    got = out[torch.from_numpy(idx).cuda()].cpu().numpy()
+    assert_bitwise(got, want, "len > 2^31 stacked")
+    # the fused all-reduce in place, on the same data
+    arenas = [d[0], d[1]]
+    df.detfold_loopback_allreduce(arenas, 2, n, 0.5)
+    torch.cuda.synchronize()
+    want_ar = oracle.scale(want, np.float32(0.5))
+    ti = torch.from_numpy(idx).cuda()
+    for r in range(2):
+        assert_bitwise(arenas[r][ti].cpu().numpy(), want_ar, f"len > 2^31 all-reduce rank {r}")
+    assert df.detfold_pipeline_timeouts() == 0

@@ -416,9 +416,10 @@ int detfold_last_cuda_error(void) { return g_last_cuda_error; }
 int detfold_pipeline_timeouts(int64_t *count)
 {
     if (!count) return DETFOLD_ERR_NULL;
-    unsigned long long c = 0;
-    if (int rc = cuda_status(detfold::read_pipeline_timeouts(&c))) return rc;
-    *count = (int64_t)c;
+    unsigned long long a = 0, b = 0;
+    if (int rc = cuda_status(detfold::read_pipeline_timeouts_bulk(&a))) return rc;
+    if (int rc = cuda_status(detfold::read_pipeline_timeouts_move(&b))) return rc;
+    *count = (int64_t)(a + b);
     return DETFOLD_OK;
 }
 

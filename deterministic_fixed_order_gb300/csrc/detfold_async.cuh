@@ -1,0 +1,107 @@
+// Bulk-async (TMA) building blocks for the staged pipelines: mbarrier
+// set-up, arrival and bounded waits, cp.async.bulk loads (global -> shared,
+// completion by byte count on an mbarrier) and stores (shared -> global, in
+// bulk groups), and the proxy fence between generic shared-memory writes and
+// a bulk store. Every wait is bounded; an expiry is counted in
+// g_pipeline_timeouts. Each translation unit that includes this header has
+// its own counter (internal linkage: device code is compiled per unit) and
+// exports a reader; detfold_pipeline_timeouts sums them.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace detfold {
+
+static __device__ unsigned long long g_pipeline_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ long long now_ns()
+{
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.
+static __device__ bool mbar_wait(uint64_t *b, uint32_t parity)
+{
+    const long long t0 = now_ns();
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (mbar_try(b, parity)) return true;
+        if (now_ns() - t0 > 1000000000LL) break;
+    }
+    atomicAdd(&g_pipeline_timeouts, 1ull);
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void named_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Host side: this translation unit's counter.
+static inline cudaError_t read_unit_timeouts(unsigned long long *count)
+{
+    return cudaMemcpyFromSymbol(count, g_pipeline_timeouts, sizeof(*count));
+}
+
+}  // namespace detfold

@@ -67,6 +67,9 @@
 #ifndef DETFOLD_USE_BULK
 #define DETFOLD_USE_BULK 1  // bulk-async (TMA) staged path for large aligned calls
 #endif
+#ifndef DETFOLD_USE_BULK_MOVE
+#define DETFOLD_USE_BULK_MOVE 1  // bulk-async path for large pure-movement launches
+#endif
 #ifndef DETFOLD_BULK_MIN_LEN
 #define DETFOLD_BULK_MIN_LEN (1 << 20)  // elements at or above: the bulk path
 #endif

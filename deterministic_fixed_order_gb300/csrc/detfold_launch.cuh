@@ -144,7 +144,8 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
 // Bulk-async (TMA) staged bandwidth path (fold_bulk.cu).
 int bulk_tile_floats(int W);
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream);
-cudaError_t read_pipeline_timeouts(unsigned long long *count);
+cudaError_t read_pipeline_timeouts_bulk(unsigned long long *count);
+cudaError_t read_pipeline_timeouts_move(unsigned long long *count);
 
 template <int W, int MODE>
 inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)

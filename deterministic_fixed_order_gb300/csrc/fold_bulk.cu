@@ -28,96 +28,12 @@
 #include <cuda_runtime.h>
 
 #include "detfold.h"
+#include "detfold_async.cuh"
 #include "detfold_launch.cuh"
 
 namespace detfold {
 
 namespace {
-
-__device__ unsigned long long g_pipeline_timeouts;
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ long long now_ns()
-{
-    long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect(uint64_t *b, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_addr(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase of parity `parity` to complete.
-__device__ bool mbar_wait(uint64_t *b, uint32_t parity)
-{
-    const long long t0 = now_ns();
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
-        if (mbar_try(b, parity)) return true;
-        if (now_ns() - t0 > 1000000000LL) break;
-    }
-    atomicAdd(&g_pipeline_timeouts, 1ull);
-    return false;
-}
-
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_addr(src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void named_sync(int id, int n)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // Tile shapes from GB300 sweeps: 8 KB per rank and 3 stages up to W = 4,
 // 4 KB per rank and 2 stages above; four consumer warps.
@@ -328,6 +244,8 @@ cudaError_t launch_bulk_mode(const LaunchSpec &s, int64_t head, cudaStream_t str
 
 }  // namespace
 
+cudaError_t read_pipeline_timeouts_bulk(unsigned long long *count) { return read_unit_timeouts(count); }
+
 int bulk_tile_floats(int W) { return W <= 4 ? BulkShape<4>::T : BulkShape<8>::T; }
 
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream)
@@ -336,9 +254,5 @@ cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream)
     return launch_bulk_mode<kSumCoherent>(s, head, stream);
 }
 
-cudaError_t read_pipeline_timeouts(unsigned long long *count)
-{
-    return cudaMemcpyFromSymbol(count, g_pipeline_timeouts, sizeof(*count));
-}
 
 }  // namespace detfold

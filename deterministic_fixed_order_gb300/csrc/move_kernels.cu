@@ -12,14 +12,141 @@
 // Each thread loads the vectors of up to G pairs before storing any of them.
 // Sources are read through the read-only path: the API layer guarantees that
 // no destination overlaps any source of the same launch.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "detfold_async.cuh"
 #include "detfold_launch.cuh"
 
 namespace detfold {
 
 namespace {
+
+// ---------------------------------------------------------------- bulk-async movement
+
+// Large aligned moves: one loader lane streams a tile of every distinct
+// source (consecutive pairs with the same source share it) into a ring of
+// shared-memory stages with cp.async.bulk; one storer lane issues a bulk
+// store per destination straight from shared memory, so a source with
+// several destinations (a distribute phase, a broadcast) is read from DRAM
+// once. A stage is released only after the stores reading it have finished
+// reading (wait_group.read). Waits are bounded (detfold_async.cuh).
+template <int G>
+struct MoveShape {
+    static constexpr int T = 2048;              // floats per source per tile (8 KB)
+    static constexpr int S = G <= 4 ? 4 : 2;    // stages
+    static constexpr size_t SMEM = (size_t)S * G * T * 4 + 2 * S * 8;
+};
+
+template <int G>
+struct MoveBulkParams {
+    const float *src[G];           // distinct sources
+    float *dst[kMaxPairs];         // destinations in pair order
+    unsigned char grp[kMaxPairs];  // pair -> source slot
+    int K;
+    int64_t len, head, ntiles;
+};
+
+template <int G>
+__global__ void __launch_bounds__(64) move_bulk_kernel(const __grid_constant__ MoveBulkParams<G> p)
+{
+    using Sh = MoveShape<G>;
+    constexpr int T = Sh::T, S = Sh::S;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float *buf = (float *)smem;  // [S][G][T]
+    uint64_t *full = (uint64_t *)(buf + (size_t)S * G * T);
+    uint64_t *empty = full + S;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // loader
+        long long k = 0;
+        for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
+            const int s = (int)(k % S);
+            if (k >= S && !mbar_wait(&empty[s], (uint32_t)(((k / S) - 1) & 1))) break;
+            mbar_arrive_expect(&full[s], G * T * 4);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                bulk_load(buf + ((size_t)s * G + g) * T, p.src[g] + p.head + t * T, T * 4, &full[s]);
+        }
+        for (long long j = (k > S ? k - S : 0); j < k; ++j)  // own copies landed
+            if (!mbar_wait(&full[j % S], (uint32_t)((j / S) & 1))) break;
+        return;
+    }
+    if (threadIdx.x == 32) {  // storer
+        long long k = 0;
+        for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) break;
+            const int64_t e = p.head + t * T;
+            for (int q = 0; q < p.K; ++q) bulk_store(p.dst[q] + e, buf + ((size_t)s * G + p.grp[q]) * T, T * 4);
+            bulk_commit();
+            if (k >= 1) {
+                bulk_wait_read<1>();              // stores of tile k-1 have read their stage
+                mbar_arrive(&empty[(k - 1) % S]);
+            }
+        }
+        bulk_wait_all();
+    } else if (threadIdx.x > 32 && blockIdx.x == gridDim.x - 1) {
+        // head [0, head) and tail [head + ntiles*T, len), scalar, by 31 lanes
+        const int64_t tail0 = p.head + p.ntiles * T;
+        const int64_t nhead = p.head, ntail = p.len - tail0;
+        for (int64_t q = threadIdx.x - 33; q < nhead + ntail; q += 31) {
+            const int64_t i = q < nhead ? q : tail0 + (q - nhead);
+            for (int k = 0; k < p.K; ++k) st1(p.dst[k] + i, ld1<true>(p.src[p.grp[k]] + i));
+        }
+    }
+}
+
+template <int G>
+cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, int K, int64_t len,
+                                   int64_t head, cudaStream_t stream)
+{
+    using Sh = MoveShape<G>;
+    MoveBulkParams<G> p = {};
+    int g = -1;
+    for (int k = 0; k < K; ++k) {
+        if (k == 0 || src[k] != src[k - 1]) p.src[++g] = src[k];
+        p.dst[k] = dst[k];
+        p.grp[k] = (unsigned char)g;
+    }
+    p.K = K;
+    p.len = len;
+    p.head = head;
+    p.ntiles = (len - head) / Sh::T;
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int cap = cache[dev].load(std::memory_order_relaxed);
+    if (cap <= 0) {
+        e = cudaFuncSetAttribute(move_bulk_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, move_bulk_kernel<G>, 64, Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        if (per_sm > 4) per_sm = 4;
+        cap = sms * (per_sm > 0 ? per_sm : 1);
+        cache[dev].store(cap, std::memory_order_relaxed);
+    }
+    int64_t grid = p.ntiles < cap ? p.ntiles : cap;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(64, 1, 1);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, move_bulk_kernel<G>, p);
+}
 
 template <int VEC>
 __global__ void __launch_bounds__(256) move_pairs_kernel(const __grid_constant__ MoveParams p)
@@ -79,6 +206,28 @@ int elem_phase_any(const void *q, int vec) { return (int)(((uintptr_t)q % (uintp
 static cudaError_t launch_move_chunk(const float *const *src, float *const *dst, int K,
                                      int64_t len, cudaStream_t stream)
 {
+    // bulk-async path: large, every operand at one 16-byte phase, <= 8 distinct sources
+    if (DETFOLD_USE_BULK && DETFOLD_USE_BULK_MOVE && len >= DETFOLD_BULK_MIN_LEN) {
+        int groups = 0;
+        for (int k = 0; k < K; ++k) groups += (k == 0 || src[k] != src[k - 1]);
+        const int ph = elem_phase_any(src[0], 4);
+        bool same = true;
+        for (int k = 0; same && k < K; ++k)
+            same = elem_phase_any(src[k], 4) == ph && elem_phase_any(dst[k], 4) == ph;
+        const int64_t head = (4 - ph) % 4;
+        if (same && groups <= 8 && len - head >= MoveShape<1>::T) {
+            switch (groups) {
+            case 1: return launch_move_bulk_fixed<1>(src, dst, K, len, head, stream);
+            case 2: return launch_move_bulk_fixed<2>(src, dst, K, len, head, stream);
+            case 3: return launch_move_bulk_fixed<3>(src, dst, K, len, head, stream);
+            case 4: return launch_move_bulk_fixed<4>(src, dst, K, len, head, stream);
+            case 5: return launch_move_bulk_fixed<5>(src, dst, K, len, head, stream);
+            case 6: return launch_move_bulk_fixed<6>(src, dst, K, len, head, stream);
+            case 7: return launch_move_bulk_fixed<7>(src, dst, K, len, head, stream);
+            default: return launch_move_bulk_fixed<8>(src, dst, K, len, head, stream);
+            }
+        }
+    }
     MoveParams p = {};
     for (int k = 0; k < K; ++k) {
         p.src[k] = src[k];
@@ -119,5 +268,7 @@ cudaError_t launch_move(const float *const *src, float *const *dst, int K, int64
     }
     return cudaSuccess;
 }
+
+cudaError_t read_pipeline_timeouts_move(unsigned long long *count) { return read_unit_timeouts(count); }
 
 }  // namespace detfold

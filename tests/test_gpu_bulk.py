@@ -74,3 +74,53 @@ def test_bulk_repeated_calls_and_no_pipeline_timeouts():
     for r in range(W):
         assert_bitwise(arenas[r].host(), host[r], f"repeated bulk all-reduce rank {r}")
     assert df.detfold_pipeline_timeouts() == 0
+
+
+def _bits_rows(W, n, seed):
+    return np.random.default_rng(seed).integers(0, 2 ** 32, size=(W, n), dtype=np.uint64) \
+        .astype(np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("n", [M, M + 5, 3 * M + 2049])
+@pytest.mark.parametrize("nd", [1, 3, 7])
+def test_bulk_broadcast_moves_bytes_exactly(n, nd):
+    src_h = _bits_rows(1, n, n + nd)[0]
+    src = Guarded(n, 2, src_h)
+    dsts = [Guarded(n, 2) for _ in range(nd)]
+    df.detfold_broadcast([d.t for d in dsts], nd, src.t, n)
+    torch.cuda.synchronize()
+    for k, d in enumerate(dsts):
+        assert_bitwise(d.host(), src_h, f"bulk broadcast n={n} dst={k}")
+        assert d.intact()
+
+
+@pytest.mark.parametrize("W", [2, 4, 5, 8])
+def test_bulk_all_gather_and_staged(W):
+    span = M + 4  # keeps every part's offset at the same 16-byte phase
+    parts_h = _bits_rows(W, span, 100 + W)
+    parts = [Guarded(span, 0, parts_h[r]) for r in range(W)]
+    outs = [Guarded(W * span, 0) for _ in range(W)]
+    df.detfold_all_gather([o.t for o in outs], W, [p.t for p in parts], span)
+    torch.cuda.synchronize()
+    want = parts_h.reshape(-1)
+    for r, o in enumerate(outs):
+        assert_bitwise(o.host(), want, f"bulk all-gather W={W} rank={r}")
+        assert o.intact()
+    # the staged comparator with shards of at least 2^20: bulk exchange and distribute
+    n = W * M + 13
+    rows = gen.normal_rows(W, n)
+    arenas = [Guarded(n, 1, rows[r]) for r in range(W)]
+    nb = df.detfold_staged_workspace_bytes(n, W)
+    ws = torch.empty(nb // 4, dtype=torch.float32, device="cuda")
+    scale = float(oracle.mean_scale(W))
+    for flags in (0, 1, 2):
+        for r in range(W):
+            arenas[r].t.copy_(torch.from_numpy(rows[r]))
+        df.detfold_loopback_allreduce_staged([a.t for a in arenas], W, n, scale, flags, ws, nb)
+        torch.cuda.synchronize()
+        want = [rows[r].copy() for r in range(W)]
+        oracle.allreduce(want, np.float32(scale))
+        for r in range(W):
+            assert_bitwise(arenas[r].host(), want[r], f"bulk staged W={W} flags={flags} rank={r}")
+            assert arenas[r].intact()
+    assert df.detfold_pipeline_timeouts() == 0

@@ -68,7 +68,7 @@ NCU_TRAFFIC = {
                                          "kernel_hash": "ed371981487c166c"},
 }
 
-KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "fold_sum_nc.cu",
+KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",
                 "fold_sum_coherent.cu", "fold_allreduce.cu", "fold_bulk.cu")
 
 

@@ -76,6 +76,9 @@
 #ifndef DETFOLD_SMALL_PDL
 #define DETFOLD_SMALL_PDL 1  // programmatic dependent launch on the small path
 #endif
+#ifndef DETFOLD_PDL_ALL
+#define DETFOLD_PDL_ALL 1  // programmatic dependent launch on every launch
+#endif
 #ifndef DETFOLD_SUM_CTAS_PER_SM
 #define DETFOLD_SUM_CTAS_PER_SM 1  // 0: as many as fit; else at most this many per SM
 #endif

@@ -91,9 +91,10 @@ inline cudaError_t resident_ctas(int threads, int cap_per_sm, int *out)
     return cudaSuccess;
 }
 
-// One launch: the small path covers the work exactly with small CTAs and
-// programmatic dependent launch; the bandwidth path runs a grid of at most
-// the resident CTAs, each thread striding over U-vector groups.
+// One launch: the small path covers the work exactly with small CTAs; the
+// bandwidth path runs a grid of at most the resident CTAs, each thread
+// striding over U-vector groups. Programmatic dependent launch is used
+// exactly when the parameter block's pdl flag is set.
 template <auto Kernel, typename Params>
 inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool small, int bw_threads,
                                  int cap_per_sm, cudaStream_t stream)
@@ -116,7 +117,9 @@ inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool smal
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    if (small && DETFOLD_SMALL_PDL) {
+    // the launch attribute follows the kernel's own flag, so a kernel
+    // launched early always waits (griddepcontrol.wait) before its loads
+    if (p.pdl) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
@@ -137,7 +140,7 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
     p.scale = s.scale;
     p.do_scale = s.do_scale;
     p.W = s.W;
-    p.pdl = (small && DETFOLD_SMALL_PDL) ? 1 : 0;
+    p.pdl = ((small && DETFOLD_SMALL_PDL) || DETFOLD_PDL_ALL) ? 1 : 0;
     return p;
 }
 

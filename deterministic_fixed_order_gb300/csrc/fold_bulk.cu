@@ -71,6 +71,7 @@ struct BulkParams {
     int64_t len, head, ntiles;
     float scale;
     int do_scale;
+    int pdl;
 };
 
 template <int W, int MODE>
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const 
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    pdl_enter(p.pdl);
     __syncthreads();
 
     if (threadIdx.x < 32) {  // producer warp: one lane issues the loads
@@ -214,6 +216,7 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
     p.ntiles = (s.len - head) / Sh::T;
     p.scale = s.scale;
     p.do_scale = s.do_scale;
+    p.pdl = DETFOLD_PDL_ALL ? 1 : 0;
     int cap = 0;
     cudaError_t e = bulk_grid<W, MODE>(&cap);
     if (e != cudaSuccess) return e;
@@ -224,6 +227,13 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
     cfg.blockDim = dim3(Sh::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Sh::SMEM;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, fold_bulk_kernel<W, MODE>, p);
 }
 

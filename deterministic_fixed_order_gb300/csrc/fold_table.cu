@@ -267,7 +267,7 @@ cudaError_t launch_table(const float *const *d_table, float *out, int *d_status,
     p.do_scale = do_scale;
     p.W = W;
     const bool small = len <= DETFOLD_SMALL_LEN;
-    p.pdl = (small && DETFOLD_SMALL_PDL) ? 1 : 0;
+    p.pdl = ((small && DETFOLD_SMALL_PDL) || DETFOLD_PDL_ALL) ? 1 : 0;
     const int64_t work = (len + 7) / 8 > 0 ? (len + 7) / 8 : 1;  // vectors if 32-byte access
     // Small payloads: the register-table kernel (shortest dependent chain).
     // Bandwidth-sized calls: the shared-memory table kernel (fewer registers).

@@ -45,6 +45,7 @@ struct MoveBulkParams {
     float *dst[kMaxPairs];         // destinations in pair order
     unsigned char grp[kMaxPairs];  // pair -> source slot
     int K;
+    int pdl;
     int64_t len, head, ntiles;
 };
 
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(64) move_bulk_kernel(const __grid_constant__ M
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    pdl_enter(p.pdl);
     __syncthreads();
     if (threadIdx.x == 0) {  // loader
         long long k = 0;
@@ -117,6 +119,7 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
         p.grp[k] = (unsigned char)g;
     }
     p.K = K;
+    p.pdl = DETFOLD_PDL_ALL ? 1 : 0;
     p.len = len;
     p.head = head;
     p.ntiles = (len - head) / Sh::T;
@@ -145,6 +148,13 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
     cfg.blockDim = dim3(64, 1, 1);
     cfg.dynamicSmemBytes = Sh::SMEM;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, move_bulk_kernel<G>, p);
 }
 
@@ -236,7 +246,7 @@ static cudaError_t launch_move_chunk(const float *const *src, float *const *dst,
     p.K = K;
     p.len = len;
     const bool small = len <= DETFOLD_SMALL_LEN;
-    p.pdl = (small && DETFOLD_SMALL_PDL) ? 1 : 0;
+    p.pdl = ((small && DETFOLD_SMALL_PDL) || DETFOLD_PDL_ALL) ? 1 : 0;
     int vec = 0;
     for (int cand : {8, 4}) {
         const int ph = elem_phase_any(src[0], cand);

@@ -61,11 +61,11 @@ GRAPH_NODES = 10_000
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147698688 + 258952448,
-                                  "kernel_hash": "ed371981487c166c"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147522560 + 259438336,
+                                  "kernel_hash": "51bf94e747b1c16e"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600028160 + 1538253568,
-                                         "kernel_hash": "ed371981487c166c"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600030208 + 1538270976,
+                                         "kernel_hash": "51bf94e747b1c16e"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",

@@ -34,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -62,23 +63,31 @@ NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
     "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147522560 + 259438336,
-                                  "kernel_hash": "51bf94e747b1c16e"},
+                                  "kernel_hash": "9312bae14133dded"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
     "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600030208 + 1538270976,
-                                         "kernel_hash": "51bf94e747b1c16e"},
+                                         "kernel_hash": "9312bae14133dded"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",
                 "fold_sum_coherent.cu", "fold_allreduce.cu", "fold_bulk.cu")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments or whitespace: what a capture depends on."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the fold kernels and their launch configuration."""
+    """Hash of the fold kernels and their launch configuration (code only:
+    editing a comment does not invalidate a profile)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "deterministic_fixed_order_gb300", "csrc")
     for f in KERNEL_FILES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,14 +1,24 @@
-// Device side of libdetfold: the fixed-order fold kernels for sm_103a.
+// Device side of libdetfold: the vector fold kernels for sm_103a.
 //
-// One kernel family covers every fold of the library. Each thread owns whole
-// output elements; for each it loads the W addends (all loads of an unrolled
-// group are issued before any add), then runs the serial chain
-//     acc = s_0; acc = __fadd_rn(acc, s_r) for r = 1..W-1
+// Every fold of the library computes, per element i, the serial chain
+//     acc = s_0[i]; acc = __fadd_rn(acc, s_r[i]) for r = 1..W-1
 // in ascending source-rank order (mamba-rs 0.6.2 src/dist/reducer.rs,
 // `DET_SUM_RANKS_SRC` and `reduce_sum_reference`), optionally multiplies by
 // the mean scale with one __fmul_rn (module doc of the same page), and stores.
 // No lane ever combines values of another element, so the bits do not depend
-// on the grid, the vector width or the unroll depth.
+// on the kernel, the grid, the vector width or the unroll depth.
+//
+// This header holds the load-into-registers kernels:
+//   fold_vec_kernel       W <= 8, every operand at one 32- or 16-byte phase:
+//                         scalar head, vector body (all loads of a group
+//                         issued before any add), scalar tail;
+//   fold_realign_kernel   sums whose sources sit at different 4-byte phases:
+//                         vectors on the output's grid, straddles rebuilt
+//                         with warp shuffles;
+//   fold_scalar_kernel    the all-reduce at mismatched phases;
+//   fold_vec/scalar_generic_kernel   8 < W <= 256.
+// Large aligned calls take the bulk-async (TMA) kernels of fold_bulk.cu;
+// device-resident pointer tables take fold_table.cu.
 //
 // Modes:
 //   kSumNC        out <- fold(src); sources read through the read-only path
@@ -18,16 +28,10 @@
 //   kAllReduce    every arena <- fold(arenas); ordinary loads, then W stores
 //                 (each element is read, then written, by the same thread).
 //
-// Layout: `head` scalar elements until every operand reaches a VEC*4-byte
-// boundary, `nvec` vectors of VEC floats, then a scalar tail. When operands
-// do not share one phase the scalar kernel runs instead (coalesced 4-byte
-// accesses with U*W loads in flight per thread).
-//
-// The small-payload path launches the same kernels with programmatic
-// dependent launch: `griddepcontrol.wait` before the first load (inputs may
-// come from the preceding kernel), `griddepcontrol.launch_dependents` right
-// after, so the next fold's CTAs are resident when this one retires. There
-// are no spin waits of any kind.
+// Every launch uses programmatic dependent launch: a kernel executes
+// `griddepcontrol.wait` before its first load (its inputs may come from the
+// preceding kernel) and `griddepcontrol.launch_dependents` right after, so
+// the next grid is resident when this one retires. There are no spin waits.
 #pragma once
 
 #include <cstdint>
@@ -77,7 +81,7 @@
 #define DETFOLD_SMALL_PDL 1  // programmatic dependent launch on the small path
 #endif
 #ifndef DETFOLD_PDL_ALL
-#define DETFOLD_PDL_ALL 1  // programmatic dependent launch on every launch
+#define DETFOLD_PDL_ALL 1  // ... and on every other launch (0 restricts it to the small path)
 #endif
 #ifndef DETFOLD_SUM_CTAS_PER_SM
 #define DETFOLD_SUM_CTAS_PER_SM 1  // 0: as many as fit; else at most this many per SM

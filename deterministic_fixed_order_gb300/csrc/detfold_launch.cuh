@@ -1,6 +1,8 @@
-// Host-side launch plumbing shared by the three mode translation units:
-// phase planning (vector width, head, body, tail), grid sizing, and the
-// typed launch of one kernel instantiation.
+// Host-side launch plumbing shared by the mode translation units: phase
+// planning (vector width, head, body, tail), grid sizing, the typed launch
+// of one kernel instantiation, and the dispatch order of a fold call:
+// bulk-async path (large, aligned, W <= 8) -> vector kernel (common phase) ->
+// realigned vectors (sums at mismatched phases) -> scalar kernel.
 #pragma once
 
 #include <atomic>

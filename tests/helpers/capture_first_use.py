@@ -1,0 +1,40 @@
+"""Run in a fresh process: the first use of the bulk-async, movement and
+realign kernels happens inside a CUDA-graph capture (their one-time set-up --
+shared-memory opt-in, occupancy -- runs during capture). Replays twice and
+writes the outputs for the parent test to check against the oracle."""
+import sys
+
+import numpy as np
+import torch
+
+sys.path.insert(0, sys.argv[1])
+import deterministic_fixed_order_gb300 as df  # noqa: E402
+import detfold_inputs as gen  # noqa: E402
+
+out_path = sys.argv[2]
+W, n = 4, (1 << 22) + 5
+rows = gen.stress_rows(W, n)
+st = torch.from_numpy(rows).cuda()
+out = torch.empty(n, device="cuda")
+arenas = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
+staged = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
+nb = df.detfold_staged_workspace_bytes(n, W)
+ws = torch.empty(nb // 4, device="cuda")
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+s = torch.cuda.Stream()
+with torch.cuda.graph(g, stream=s):
+    df.detfold_sum_stacked(out, st, W, n)            # stacked rows: mismatched phases -> realign
+    df.detfold_sum_ptrs(out, [st[r] for r in range(W)], W, n)   # same; ptrs
+    df.detfold_loopback_allreduce(arenas, W, n, 0.25)           # bulk all-reduce
+    df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, 0, ws, nb)  # bulk moves + folds
+for _ in range(2):
+    for r in range(W):
+        arenas[r].copy_(torch.from_numpy(rows[r]))
+        staged[r].copy_(torch.from_numpy(rows[r]))
+    g.replay()
+torch.cuda.synchronize()
+res = np.stack([out.cpu().numpy(), arenas[0].cpu().numpy(), arenas[W - 1].cpu().numpy(),
+                staged[0].cpu().numpy(), staged[W - 1].cpu().numpy()])
+np.save(out_path, res)
+print("timeouts", df.detfold_pipeline_timeouts())

@@ -124,3 +124,24 @@ def test_bulk_all_gather_and_staged(W):
             assert_bitwise(arenas[r].host(), want[r], f"bulk staged W={W} flags={flags} rank={r}")
             assert arenas[r].intact()
     assert df.detfold_pipeline_timeouts() == 0
+
+
+def test_first_use_inside_graph_capture(tmp_path):
+    # A fresh process whose first bulk/movement/realign launches are captured.
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = str(tmp_path / "res.npy")
+    r = subprocess.run([sys.executable, os.path.join(root, "tests", "helpers", "capture_first_use.py"),
+                        root, out], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    assert "timeouts 0" in r.stdout
+    res = np.load(out)
+    W, n = 4, (1 << 22) + 5
+    rows = gen.stress_rows(W, n)
+    assert_bitwise(res[0], oracle.fold(rows), "captured ptrs fold")
+    want = [rows[q].copy() for q in range(W)]
+    oracle.allreduce(want, np.float32(0.25))
+    for k, q in ((1, 0), (2, W - 1), (3, 0), (4, W - 1)):
+        assert_bitwise(res[k], want[q], f"captured all-reduce result {k}")

@@ -21,7 +21,7 @@ L2, so no L2 flush is needed between steps.
 Also reported: per-row kernel times from CUDA events on the launching
 stream, the roofline of the dominant kernel, microseconds per call of the
 16 KiB W=2 fold inside a 10,000-node CUDA graph (with the empty-kernel
-floor), an end-to-end figure through the public API with host buffers, SM
+and the one-warp memory round-trip floors), an end-to-end figure through the public API with host buffers, SM
 clocks sampled during the run, a sampled bit-exact check of the bench's own
 outputs against the CPU oracle, and the oracle timed on host cores.
 
@@ -371,6 +371,11 @@ def graph_us_per_call(torch, df, wl, n: int, reps: int = 25) -> dict:
     del g
     g = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 0))
     res["floor_us_plain"] = time_graph(g)
+    del g
+    # a one-warp load-after-predecessor + store: the least a dependent fold can take
+    pair = torch.zeros(64, device="cuda")
+    g = capture(lambda: df.detfold_memory_floor(pair[:32], pair[32:], GRAPH_NODES, 1))
+    res["floor_us_memory_pdl"] = time_graph(g)
     del g
     return res
 

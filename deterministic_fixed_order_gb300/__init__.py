@@ -28,7 +28,7 @@ __all__ = [
     "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
     "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_noalloc",
     "detfold_shard_plan", "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
-    "STATUS",
+    "detfold_memory_floor", "STATUS",
 ]
 
 LIB_PATH = _build.LIB
@@ -82,6 +82,7 @@ lib.detfold_status_string.argtypes = [_INT]
 lib.detfold_status_string.restype = ctypes.c_char_p
 lib.detfold_last_cuda_error.argtypes = []
 lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
+lib.detfold_memory_floor.argtypes = [_P, _P, _INT, _INT, _P]
 lib.detfold_pipeline_timeouts.argtypes = [_P]
 for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
@@ -89,7 +90,7 @@ for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
               "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
               "detfold_one_shot_allreduce",
               "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor",
-              "detfold_pipeline_timeouts"):
+              "detfold_memory_floor", "detfold_pipeline_timeouts"):
     getattr(lib, _name).restype = _INT
 
 
@@ -388,6 +389,13 @@ def detfold_pipeline_timeouts() -> int:
 
 def detfold_launch_floor(count: int, pdl: int = 1, stream=None) -> None:
     _check(lib.detfold_launch_floor(count, pdl, _stream(stream)), "detfold_launch_floor")
+
+
+def detfold_memory_floor(src, dst, count: int, pdl: int = 1, stream=None) -> None:
+    """`count` one-warp launches, each copying src[0:32] to dst[0:32] after
+    the preceding grid retires."""
+    _check(lib.detfold_memory_floor(_dev_ptr(src, 32, "src"), _dev_ptr(dst, 32, "dst"), count, pdl,
+                                    _stream(stream)), "detfold_memory_floor")
 
 
 # ------------------------------------------------------------------ tensor conveniences

@@ -84,12 +84,14 @@ int arenas_valid(float *const *arenas, int W, int64_t len)
     return DETFOLD_OK;
 }
 
-__global__ void empty_kernel(int pdl)
+__global__ void empty_kernel(int pdl) { detfold::pdl_enter(pdl); }
+
+// One warp: each lane copies one float, loaded only after the preceding
+// grid has retired (the same dependency a fold launch has on its inputs).
+__global__ void copy_warp_kernel(const float *__restrict__ src, float *__restrict__ dst, int pdl)
 {
-    if (pdl) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    }
+    detfold::pdl_enter(pdl);
+    dst[threadIdx.x] = src[threadIdx.x];
 }
 
 }  // namespace
@@ -100,7 +102,11 @@ namespace detfold {
 // defined in other translation units).
 int record_cuda_status(cudaError_t e) { return cuda_status(e); }
 
-cudaError_t launch_empty(int count, int pdl, cudaStream_t stream)
+// `count` launches of a one-warp kernel, with programmatic dependent launch
+// exactly when pdl != 0 (as the small-payload fold path launches).
+template <typename... Params, typename... Args>
+static cudaError_t launch_floor_kernel(void (*kernel)(Params...), int count, int pdl, cudaStream_t stream,
+                                      Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
@@ -114,10 +120,20 @@ cudaError_t launch_empty(int count, int pdl, cudaStream_t stream)
         cfg.numAttrs = 1;
     }
     for (int k = 0; k < count; ++k) {
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, empty_kernel, pdl);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_empty(int count, int pdl, cudaStream_t stream)
+{
+    return launch_floor_kernel(empty_kernel, count, pdl, stream, pdl);
+}
+
+cudaError_t launch_copy_warp(const float *src, float *dst, int count, int pdl, cudaStream_t stream)
+{
+    return launch_floor_kernel(copy_warp_kernel, count, pdl, stream, src, dst, pdl);
 }
 
 }  // namespace detfold
@@ -427,6 +443,15 @@ int detfold_launch_floor(int count, int pdl, void *stream)
 {
     if (count < 0) return DETFOLD_ERR_ARG;
     return cuda_status(detfold::launch_empty(count, pdl ? 1 : 0, (cudaStream_t)stream));
+}
+
+int detfold_memory_floor(const float *src, float *dst, int count, int pdl, void *stream)
+{
+    if (!src || !dst) return DETFOLD_ERR_NULL;
+    if (count < 0) return DETFOLD_ERR_ARG;
+    if (!aligned4(src) || !aligned4(dst)) return DETFOLD_ERR_ALIGN;
+    if (intersects(src, 32 * sizeof(float), dst, 32 * sizeof(float))) return DETFOLD_ERR_OVERLAP;
+    return cuda_status(detfold::launch_copy_warp(src, dst, count, pdl ? 1 : 0, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -9,6 +9,8 @@
 // on the kernel, the grid, the vector width or the unroll depth.
 //
 // This header holds the load-into-registers kernels:
+//   fold_small_kernel     W <= 8, len <= DETFOLD_SMALL_LEN, one phase: one
+//                         vector per thread, head and tail out of line;
 //   fold_vec_kernel       W <= 8, every operand at one 32- or 16-byte phase:
 //                         scalar head, vector body (all loads of a group
 //                         issued before any add), scalar tail;
@@ -59,6 +61,9 @@
 #ifndef DETFOLD_SMALL_LEN
 #define DETFOLD_SMALL_LEN (1 << 17)  // elements at or below: small-payload launch
 #endif
+#ifndef DETFOLD_SMALL_VEC
+#define DETFOLD_SMALL_VEC DETFOLD_PREFER_VEC  // widest vector on the small path
+#endif
 #ifndef DETFOLD_SMALL_THREADS
 #define DETFOLD_SMALL_THREADS 128
 #endif
@@ -82,6 +87,9 @@
 #endif
 #ifndef DETFOLD_PDL_ALL
 #define DETFOLD_PDL_ALL 1  // ... and on every other launch (0 restricts it to the small path)
+#endif
+#ifndef DETFOLD_PDL_TRIGGER_FIRST
+#define DETFOLD_PDL_TRIGGER_FIRST 0  // 1: launch_dependents before the wait instead of after
 #endif
 #ifndef DETFOLD_SUM_CTAS_PER_SM
 #define DETFOLD_SUM_CTAS_PER_SM 1  // 0: as many as fit; else at most this many per SM
@@ -147,6 +155,7 @@ struct FoldParams {
     int do_scale;
     int W;                 // runtime world size (used by the generic kernels)
     int pdl;               // launched with programmatic dependent launch
+    int edges;             // the call has a head or a tail (small-payload kernel)
 };
 
 // Pure-movement launches: K (source -> destination) pairs of equal length.
@@ -226,11 +235,19 @@ __device__ __forceinline__ void stv(float *p, const Vec<VEC> &x)
                      : "memory");
 }
 
+// Either order is correct: launch_dependents only lets the next grid be
+// scheduled; that grid's own wait still blocks until this grid has retired
+// and its writes are visible.
 __device__ __forceinline__ void pdl_enter(int pdl)
 {
     if (pdl) {
+#if DETFOLD_PDL_TRIGGER_FIRST
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+#else
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
     }
 }
 
@@ -321,6 +338,45 @@ __global__ void __launch_bounds__(max_threads<MODE>()) fold_vec_kernel(const __g
     const int64_t tail0 = p.head + p.nvec * VEC;
     if (gtid < p.head) fold_one<W, MODE>(p, gtid);
     if (gtid < p.len - tail0) fold_one<W, MODE>(p, tail0 + gtid);
+}
+
+// ---------------------------------------------------------------- small-payload kernel, fixed W
+
+// The head and the tail of a small call (fewer than VEC elements each), out
+// of line: only the first VEC threads of the grid enter it, and only when the
+// call has any.
+template <int W, int VEC, int MODE>
+__device__ __noinline__ void fold_edges(const FoldParams<W> &p, int i)
+{
+    const int head = (int)p.head, tail0 = head + (int)p.nvec * VEC;
+    if (i < head) fold_one<W, MODE>(p, i);
+    if (i < (int)p.len - tail0) fold_one<W, MODE>(p, tail0 + i);
+}
+
+// The small path (len <= DETFOLD_SMALL_LEN), every operand at one phase: one
+// vector per thread, no loop, 32-bit indices. Back to back in a graph, such
+// a launch costs about what its CTAs execute after the wait, so the body is
+// only the W loads, the chain and the store.
+template <int W, int VEC, int MODE>
+__global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) fold_small_kernel(const __grid_constant__ FoldParams<W> p)
+{
+    static_assert(DETFOLD_SMALL_LEN < (1 << 30), "small-path indices are 32-bit");
+    constexpr bool NC = (MODE == kSumNC);
+    pdl_enter(p.pdl);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < (int)p.nvec) {
+        const int e = (int)p.head + i * VEC;
+        Vec<VEC> x[W];
+#pragma unroll
+        for (int r = 0; r < W; ++r) x[r] = ldv<VEC, NC>(p.src[r] + e);
+        Vec<VEC> acc = x[0];
+#pragma unroll
+        for (int r = 1; r < W; ++r)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc.v[k] = __fadd_rn(acc.v[k], x[r].v[k]);
+        store_result<VEC, W, MODE>(p, e, acc);
+    }
+    if (p.edges && i < VEC) fold_edges<W, VEC, MODE>(p, i);
 }
 
 // ---------------------------------------------------------------- scalar kernel, fixed W

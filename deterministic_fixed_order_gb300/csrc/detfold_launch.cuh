@@ -1,8 +1,9 @@
 // Host-side launch plumbing shared by the mode translation units: phase
 // planning (vector width, head, body, tail), grid sizing, the typed launch
 // of one kernel instantiation, and the dispatch order of a fold call:
-// bulk-async path (large, aligned, W <= 8) -> vector kernel (common phase) ->
-// realigned vectors (sums at mismatched phases) -> scalar kernel.
+// bulk-async path (large, aligned, W <= 8) -> small-payload kernel (small,
+// common phase) -> vector kernel (common phase) -> realigned vectors (sums at
+// mismatched phases) -> scalar kernel.
 #pragma once
 
 #include <atomic>
@@ -35,10 +36,11 @@ inline int elem_phase(const void *p, int vec)
     return (int)(((uintptr_t)p % (uintptr_t)(vec * 4)) / 4);
 }
 
-// The widest vector whose phase every operand shares (the output as well).
-inline Plan make_plan(const LaunchSpec &s)
+// The widest vector, at most `prefer` floats, whose phase every operand
+// shares (the output as well).
+inline Plan make_plan(const LaunchSpec &s, int prefer)
 {
-    const int prefs[2] = {DETFOLD_PREFER_VEC, 4};
+    const int prefs[2] = {prefer, 4};
     for (int k = 0; k < 2; ++k) {
         const int vec = prefs[k];
         const int ph = elem_phase(s.src[0], vec);
@@ -143,6 +145,7 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
     p.do_scale = s.do_scale;
     p.W = s.W;
     p.pdl = ((small && DETFOLD_SMALL_PDL) || DETFOLD_PDL_ALL) ? 1 : 0;
+    p.edges = (pl.head != 0 || s.len - pl.head - pl.nvec * pl.vec != 0) ? 1 : 0;
     return p;
 }
 
@@ -155,14 +158,16 @@ cudaError_t read_pipeline_timeouts_move(unsigned long long *count);
 template <int W, int MODE>
 inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
 {
-    const Plan pl = make_plan(s);
     const bool small = s.len <= DETFOLD_SMALL_LEN;
+    const Plan pl = make_plan(s, small ? DETFOLD_SMALL_VEC : DETFOLD_PREFER_VEC);
     if (DETFOLD_USE_BULK && !small && pl.vec >= 4 && s.len >= DETFOLD_BULK_MIN_LEN &&
         s.len - pl.head >= bulk_tile_floats(W))
         return launch_bulk(s, pl.head, stream);
     const FoldParams<W> p = fill_params<W>(s, pl, small);
     constexpr int T = bw_threads<MODE>();
     constexpr int C = ctas_per_sm_cap<MODE>();
+    if (small && pl.vec == 8) return launch_kernel<fold_small_kernel<W, 8, MODE>>(p, pl.nvec, 1, true, T, C, stream);
+    if (small && pl.vec == 4) return launch_kernel<fold_small_kernel<W, 4, MODE>>(p, pl.nvec, 1, true, T, C, stream);
     if (pl.vec == 8) {
         constexpr int U = u_for<MODE>(W, 8);
         return launch_kernel<fold_vec_kernel<W, 8, U, MODE>>(p, pl.nvec, U, small, T, C, stream);
@@ -199,8 +204,8 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
 template <int MODE>
 inline cudaError_t launch_generic(const LaunchSpec &s, cudaStream_t stream)
 {
-    const Plan pl = make_plan(s);
     const bool small = s.len <= DETFOLD_SMALL_LEN;
+    const Plan pl = make_plan(s, small ? DETFOLD_SMALL_VEC : DETFOLD_PREFER_VEC);
     const FoldParams<kGenericW> p = fill_params<kGenericW>(s, pl, small);
     constexpr int T = bw_threads<MODE>();
     constexpr int C = ctas_per_sm_cap<MODE>();
@@ -231,6 +236,7 @@ cudaError_t launch_sum_nc(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_sum_coherent(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_allreduce(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_empty(int count, int pdl, cudaStream_t stream);
+cudaError_t launch_copy_warp(const float *src, float *dst, int count, int pdl, cudaStream_t stream);
 // Fold or all-reduce over a device-resident pointer table (fold_table.cu).
 cudaError_t launch_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
                          float scale, int do_scale, int mode, cudaStream_t stream);

@@ -302,6 +302,20 @@ int detfold_pipeline_timeouts(int64_t *count);
  */
 int detfold_launch_floor(int count, int pdl, void *stream);
 
+/*
+ * Memory round-trip floor probe: enqueues `count` launches of a one-warp
+ * kernel in which lane t copies src[t] to dst[t] (t < 32), with the load
+ * issued only after the preceding grid has retired (programmatic dependent
+ * launch when pdl != 0, as detfold_launch_floor). It is the least any
+ * launch can take that reads data a predecessor may have written and then
+ * writes its own result, so it is the floor a graph of small folds is
+ * compared against, beside the empty-kernel floor.
+ *   src, dst  device, 32 floats each, 4-byte aligned, disjoint.
+ * Errors: NULL pointer -> ERR_NULL; count < 0 -> ERR_ARG; misaligned ->
+ * ERR_ALIGN; src and dst overlap -> ERR_OVERLAP.
+ */
+int detfold_memory_floor(const float *src, float *dst, int count, int pdl, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

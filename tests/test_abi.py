@@ -34,7 +34,8 @@ def test_header_declares_the_api():
     for want in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
                  "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
                  "detfold_staged_workspace_bytes", "detfold_shard_plan",
-                 "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor"):
+                 "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
+                 "detfold_memory_floor"):
         assert want in names
 
 
@@ -247,6 +248,12 @@ def test_validation_scale_and_floor(df):
     assert L.detfold_scale(A, 8, 1.0, None) == S["DETFOLD_OK"]   # scale 1: nothing enqueued
     assert L.detfold_launch_floor(-1, 1, None) == S["DETFOLD_ERR_ARG"]
     assert L.detfold_launch_floor(0, 1, None) == S["DETFOLD_OK"]
+    assert L.detfold_memory_floor(None, A, 1, 1, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_memory_floor(A, None, 1, 1, None) == S["DETFOLD_ERR_NULL"]
+    assert L.detfold_memory_floor(A, A + 128, -1, 1, None) == S["DETFOLD_ERR_ARG"]
+    assert L.detfold_memory_floor(A + 2, A + 128, 1, 1, None) == S["DETFOLD_ERR_ALIGN"]
+    assert L.detfold_memory_floor(A, A + 124, 1, 1, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert L.detfold_memory_floor(A, A + 128, 0, 1, None) == S["DETFOLD_OK"]
 
 
 @no_gpu_only

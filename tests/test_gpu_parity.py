@@ -214,6 +214,28 @@ def test_in_place_fold(W, k, n):
     assert_bitwise(srcs[kk].host(), want, f"in place W={W} k={k}")
 
 
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+@pytest.mark.parametrize("n", [1, 9, 4099, 1 << 17, (1 << 17) + 1])
+@pytest.mark.parametrize("off", [0, 1, 4, 7])
+def test_small_path_modes_with_heads_and_tails(W, n, off):
+    # Every mode of the small-payload launch (n <= 2^17 elements) with a head
+    # and a tail: the read-only sum, the in-place sum, and the fused
+    # all-reduce with the mean; n = 2^17 + 1 is the first bandwidth-path length.
+    rows = gen.stress_rows(W, n)
+    want = oracle.fold(rows)
+    assert_bitwise(run_ptrs(rows, [off] * W, off), want, f"sum W={W} n={n} off={off}")
+    srcs = [Guarded(n, off, rows[r]) for r in range(W)]
+    df.detfold_sum_ptrs(srcs[W - 1].t, [t.t for t in srcs], W, n)
+    sync()
+    assert all(t.intact() for t in srcs)
+    assert_bitwise(srcs[W - 1].host(), want, f"in place W={W} n={n} off={off}")
+    scale = float(oracle.mean_scale(W))
+    got = run_allreduce(rows, scale, [off] * W)
+    exp = oracle_allreduce(rows, scale)
+    for r in range(W):
+        assert_bitwise(got[r], exp[r], f"all-reduce W={W} n={n} off={off} r={r}")
+
+
 # ------------------------------------------------------------------ all-reduce: fused vs staged
 
 @pytest.mark.parametrize("W", [1, 2, 3, 4, 6, 8])
@@ -457,3 +479,29 @@ def test_lengths_beyond_int32():
     for r in range(2):
         assert_bitwise(arenas[r][ti].cpu().numpy(), want_ar, f"len > 2^31 all-reduce rank {r}")
     assert df.detfold_pipeline_timeouts() == 0
+
+
+# ------------------------------------------------------------------ latency-floor probes
+
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_floor_probes(pdl):
+    # The probes a graph of small folds is compared against: the empty
+    # kernel runs, and the one-warp round trip copies exactly 32 floats.
+    src = Guarded(32, 0, np.arange(1, 33, dtype=np.float32))
+    dst = Guarded(32)
+    df.detfold_launch_floor(5, pdl)
+    df.detfold_memory_floor(src.t, dst.t, 5, pdl)
+    sync()
+    assert dst.intact() and src.intact()
+    assert_bitwise(dst.host(), np.arange(1, 33, dtype=np.float32), "memory floor copy")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    dst.t.zero_()
+    sync()
+    with torch.cuda.graph(g, stream=stream):
+        df.detfold_launch_floor(20, pdl)
+        df.detfold_memory_floor(src.t, dst.t, 20, pdl)
+    g.replay()
+    sync()
+    assert dst.intact()
+    assert_bitwise(dst.host(), np.arange(1, 33, dtype=np.float32), "memory floor copy in a graph")

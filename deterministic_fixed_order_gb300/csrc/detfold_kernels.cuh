@@ -64,6 +64,9 @@
 #ifndef DETFOLD_SMALL_VEC
 #define DETFOLD_SMALL_VEC DETFOLD_PREFER_VEC  // widest vector on the small path
 #endif
+#ifndef DETFOLD_SMALL_EXACT
+#define DETFOLD_SMALL_EXACT 1  // small-path kernel without the bounds test when the grid is exact
+#endif
 #ifndef DETFOLD_SMALL_THREADS
 #define DETFOLD_SMALL_THREADS 128
 #endif
@@ -356,15 +359,16 @@ __device__ __noinline__ void fold_edges(const FoldParams<W> &p, int i)
 // The small path (len <= DETFOLD_SMALL_LEN), every operand at one phase: one
 // vector per thread, no loop, 32-bit indices. Back to back in a graph, such
 // a launch costs about what its CTAs execute after the wait, so the body is
-// only the W loads, the chain and the store.
-template <int W, int VEC, int MODE>
+// only the W loads, the chain and the store. EXACT: the grid has exactly
+// one thread per vector (nvec a multiple of the CTA size), so no bounds test.
+template <int W, int VEC, int MODE, bool EXACT>
 __global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) fold_small_kernel(const __grid_constant__ FoldParams<W> p)
 {
     static_assert(DETFOLD_SMALL_LEN < (1 << 30), "small-path indices are 32-bit");
     constexpr bool NC = (MODE == kSumNC);
     pdl_enter(p.pdl);
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < (int)p.nvec) {
+    if (EXACT || i < (int)p.nvec) {
         const int e = (int)p.head + i * VEC;
         Vec<VEC> x[W];
 #pragma unroll

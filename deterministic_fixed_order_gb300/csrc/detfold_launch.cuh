@@ -166,8 +166,14 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
     const FoldParams<W> p = fill_params<W>(s, pl, small);
     constexpr int T = bw_threads<MODE>();
     constexpr int C = ctas_per_sm_cap<MODE>();
-    if (small && pl.vec == 8) return launch_kernel<fold_small_kernel<W, 8, MODE>>(p, pl.nvec, 1, true, T, C, stream);
-    if (small && pl.vec == 4) return launch_kernel<fold_small_kernel<W, 4, MODE>>(p, pl.nvec, 1, true, T, C, stream);
+    if (small && pl.vec != 0) {
+        const bool exact = DETFOLD_SMALL_EXACT && pl.nvec > 0 && pl.nvec % DETFOLD_SMALL_THREADS == 0;
+        if (pl.vec == 8)
+            return exact ? launch_kernel<fold_small_kernel<W, 8, MODE, true>>(p, pl.nvec, 1, true, T, C, stream)
+                         : launch_kernel<fold_small_kernel<W, 8, MODE, false>>(p, pl.nvec, 1, true, T, C, stream);
+        return exact ? launch_kernel<fold_small_kernel<W, 4, MODE, true>>(p, pl.nvec, 1, true, T, C, stream)
+                     : launch_kernel<fold_small_kernel<W, 4, MODE, false>>(p, pl.nvec, 1, true, T, C, stream);
+    }
     if (pl.vec == 8) {
         constexpr int U = u_for<MODE>(W, 8);
         return launch_kernel<fold_vec_kernel<W, 8, U, MODE>>(p, pl.nvec, U, small, T, C, stream);

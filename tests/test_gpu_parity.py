@@ -215,12 +215,14 @@ def test_in_place_fold(W, k, n):
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 8])
-@pytest.mark.parametrize("n", [1, 9, 4099, 1 << 17, (1 << 17) + 1])
+@pytest.mark.parametrize("n", [1, 9, 1034, 4099, 16391, 1 << 17, (1 << 17) + 1])
 @pytest.mark.parametrize("off", [0, 1, 4, 7])
 def test_small_path_modes_with_heads_and_tails(W, n, off):
     # Every mode of the small-payload launch (n <= 2^17 elements) with a head
     # and a tail: the read-only sum, the in-place sum, and the fused
     # all-reduce with the mean; n = 2^17 + 1 is the first bandwidth-path length.
+    # 1034 at offset 1 (head 7, 128 vectors, tail 3) and 16391 at offset 1
+    # (head 7, 2048 vectors) give grids of exactly one thread per vector.
     rows = gen.stress_rows(W, n)
     want = oracle.fold(rows)
     assert_bitwise(run_ptrs(rows, [off] * W, off), want, f"sum W={W} n={n} off={off}")
@@ -234,6 +236,16 @@ def test_small_path_modes_with_heads_and_tails(W, n, off):
     exp = oracle_allreduce(rows, scale)
     for r in range(W):
         assert_bitwise(got[r], exp[r], f"all-reduce W={W} n={n} off={off} r={r}")
+
+
+@pytest.mark.parametrize("W", [2, 3, 8])
+@pytest.mark.parametrize("n,off", [(1028, 3), (1028, 0), (4096, 0), (4100, 1), (65536, 0)])
+def test_small_path_stacked_exact_and_ragged_grids(W, n, off):
+    # Stacked rows of n = 4 (mod 8) elements sit at alternating 32-byte phases,
+    # so the call takes 16-byte vectors: (1028, 3) has head 1, 256 vectors
+    # (an exact grid) and tail 3; (1028, 0) has 257 vectors (ragged grid).
+    rows = gen.stress_rows(W, n)
+    assert_bitwise(run_stacked(rows, off), oracle.fold(rows), f"stacked W={W} n={n} off={off}")
 
 
 # ------------------------------------------------------------------ all-reduce: fused vs staged

@@ -62,11 +62,11 @@ GRAPH_NODES = 10_000
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147522560 + 259438336,
-                                  "kernel_hash": "9312bae14133dded"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147557376 + 259136768,
+                                  "kernel_hash": "dba35bff09a022cb"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600030208 + 1538270976,
-                                         "kernel_hash": "9312bae14133dded"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600044288 + 1538846464,
+                                         "kernel_hash": "dba35bff09a022cb"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",
@@ -314,69 +314,62 @@ def sampled_check(wl, steps_run: int, torch, oracle, rng) -> dict:
     return res
 
 
-def graph_us_per_call(torch, df, wl, n: int, reps: int = 25) -> dict:
-    """Median replay time of a graph of GRAPH_NODES folds / GRAPH_NODES."""
+def graph_us_per_call(torch, df, wl, rounds: int = 5, reps: int = 5) -> dict:
+    """Microseconds per call of graphs of GRAPH_NODES back-to-back calls: the
+    W=2 fold at each C2 size (pointer table in the kernel parameters, and
+    through a device-resident table), beside three floors -- an empty
+    kernel with and without programmatic dependent launch, and a one-warp
+    load-after-predecessor + store. Every graph is captured first and then
+    timed round-robin (`rounds` x `reps` replays each), so a drift of the
+    GPU's state during the section shifts all of them alike; each figure
+    is the median over its replays."""
     stream = torch.cuda.Stream()
-    res = {}
 
     def capture(fn):
+        with torch.cuda.stream(stream):
+            fn()  # first use outside the capture
+        stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             fn()
-        return g
-
-    def time_graph(g):
-        ts = []
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        for _ in range(reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record()
-                g.replay()
-                b.record()
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3 / GRAPH_NODES)
-        return statistics.median(ts)
+        return g
 
-    with torch.cuda.stream(stream):
-        df.detfold_sum_stacked(wl.c2_out[n], wl.c2[n], 2, n)
-    stream.synchronize()
+    def rep(fn):
+        return lambda: [fn() for _ in range(GRAPH_NODES)]
 
-    def folds():
-        for _ in range(GRAPH_NODES):
-            df.detfold_sum_stacked(wl.c2_out[n], wl.c2[n], 2, n)
-
-    g = capture(folds)
-    res["us_per_call"] = time_graph(g)
-    del g
-    # the same fold through a device-resident pointer table (rebindable)
-    rows2 = [wl.c2[n][:n], wl.c2[n][n:]]
-    table = df.device_table(rows2)
-    with torch.cuda.stream(stream):
-        df.detfold_sum_ptrs_dev(wl.c2_out[n], table, 2, n)
-    stream.synchronize()
-
-    def table_folds():
-        for _ in range(GRAPH_NODES):
-            df.detfold_sum_ptrs_dev(wl.c2_out[n], table, 2, n)
-
-    g = capture(table_folds)
-    res["us_per_call_device_table"] = time_graph(g)
-    del g
-    g = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 1))
-    res["floor_us_pdl"] = time_graph(g)
-    del g
-    g = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 0))
-    res["floor_us_plain"] = time_graph(g)
-    del g
-    # a one-warp load-after-predecessor + store: the least a dependent fold can take
+    graphs, keep = {}, []
+    for n in C2_NS:
+        graphs[(str(n), "us_per_call")] = capture(rep(lambda n=n: df.detfold_sum_stacked(
+            wl.c2_out[n], wl.c2[n], 2, n)))
+        table = df.device_table([wl.c2[n][:n], wl.c2[n][n:]])
+        keep.append(table)
+        graphs[(str(n), "us_per_call_device_table")] = capture(rep(lambda n=n, table=table: df.detfold_sum_ptrs_dev(
+            wl.c2_out[n], table, 2, n)))
     pair = torch.zeros(64, device="cuda")
-    g = capture(lambda: df.detfold_memory_floor(pair[:32], pair[32:], GRAPH_NODES, 1))
-    res["floor_us_memory_pdl"] = time_graph(g)
-    del g
+    graphs[("floors", "empty_pdl")] = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 1))
+    graphs[("floors", "empty_plain")] = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 0))
+    graphs[("floors", "memory_pdl")] = capture(lambda: df.detfold_memory_floor(pair[:32], pair[32:],
+                                                                              GRAPH_NODES, 1))
+    times = {k: [] for k in graphs}
+    for _ in range(rounds):
+        for k, g in graphs.items():
+            for _ in range(reps):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record()
+                    g.replay()
+                    b.record()
+                b.synchronize()
+                times[k].append(a.elapsed_time(b) * 1e3 / GRAPH_NODES)
+    res = {}
+    for (group, key), ts in times.items():
+        res.setdefault(group, {})[key] = round(statistics.median(ts), 3)
+    res["floors"]["spread_us"] = round(max(max(v) - min(v) for v in times.values()), 3)
+    del graphs
     return res
 
 
@@ -616,7 +609,7 @@ def run_gpu(args) -> None:
     rng = np.random.default_rng(1234)
     check = sampled_check(wl, steps_done, torch, oracle, rng)
 
-    graph = {n: graph_us_per_call(torch, df, wl, n) for n in C2_NS}
+    graph = graph_us_per_call(torch, df, wl)
     extra_rows = next_rows(torch, df, wl)
 
     # End to end through the public API with host buffers: every step copies
@@ -734,7 +727,7 @@ def run_gpu(args) -> None:
         "value": round(value, 1),
         "unit": "GB/s",
         "pct_of_peak": round(100.0 * value / world / peak, 2),
-        "us_per_call_16KiB_W2": round(graph[4096]["us_per_call"], 3),
+        "us_per_call_16KiB_W2": graph["4096"]["us_per_call"],
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
@@ -756,7 +749,7 @@ def run_gpu(args) -> None:
         },
         "rows": per_row,
         "roofline": roofline,
-        "c2_graph": {str(n): {k: round(v, 3) for k, v in graph[n].items()} for n in C2_NS},
+        "c2_graph": graph,
         "next_rows": extra_rows,
         "copy_peak_gbs_this_run": round(copy_gbs, 1),
         "bitwise_sampled": check,

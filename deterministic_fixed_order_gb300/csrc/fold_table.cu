@@ -161,10 +161,8 @@ __global__ void __launch_bounds__(256) fold_table_kernel(const __grid_constant__
         table_scalar_body<MODE>(p, s_src);
 }
 
-// Small payloads with W <= 8: every thread reads the (broadcast) table
-// entries into registers, checks them and picks the access width itself --
-// no shared memory and no block barrier between the table load and the data
-// loads, which is what the latency of a graph of small folds is made of.
+// A small call at VEC-float width with a grid-stride loop (the 16-byte
+// path of the small kernel below).
 template <int WT, int VEC, int MODE>
 __device__ __forceinline__ void table_fixed_vec(const TableParams &p, const float *const (&src)[WT],
                                                 int64_t head)
@@ -211,46 +209,117 @@ __device__ __forceinline__ void table_fixed_vec(const TableParams &p, const floa
     }
 }
 
+// The W entries of a small call, passed by value to the out-of-line parts.
+template <int WT>
+struct SrcSet {
+    const float *p[WT];
+};
+
+// Element i of a small call with scalar accesses (its head and tail).
 template <int WT, int MODE>
-__global__ void __launch_bounds__(256) fold_table_fixed_kernel(const __grid_constant__ TableParams p)
+__device__ __forceinline__ void table_fold_one(const TableParams &p, const SrcSet<WT> &s, int i)
 {
-    pdl_enter(p.pdl);
-    const float *src[WT];
+    float acc = ld1<false>(s.p[0] + i);
 #pragma unroll
-    for (int r = 0; r < WT; ++r) src[r] = p.table[r];
-    int code = DETFOLD_OK;
+    for (int r = 1; r < WT; ++r) acc = __fadd_rn(acc, ld1<false>(s.p[r] + i));
+    if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+    if constexpr (MODE == kAllReduce) {
 #pragma unroll
-    for (int r = 0; r < WT; ++r) {
-        if (code == DETFOLD_OK && src[r] == nullptr) code = DETFOLD_ERR_NULL;
-        if (code == DETFOLD_OK && ((uintptr_t)src[r] & 3u)) code = DETFOLD_ERR_ALIGN;
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = code;
-    if (code != DETFOLD_OK) return;
-    bool same8 = (MODE == kAllReduce) || phase_of(p.out, 8) == phase_of(src[0], 8);
-    bool same4 = (MODE == kAllReduce) || phase_of(p.out, 4) == phase_of(src[0], 4);
-#pragma unroll
-    for (int r = 1; r < WT; ++r) {
-        same8 = same8 && phase_of(src[r], 8) == phase_of(src[0], 8);
-        same4 = same4 && phase_of(src[r], 4) == phase_of(src[0], 4);
-    }
-    if (same8) {
-        int64_t head = (8 - phase_of(src[0], 8)) % 8;
-        table_fixed_vec<WT, 8, MODE>(p, src, head > p.len ? p.len : head);
-    } else if (same4) {
-        int64_t head = (4 - phase_of(src[0], 4)) % 4;
-        table_fixed_vec<WT, 4, MODE>(p, src, head > p.len ? p.len : head);
+        for (int r = 0; r < WT; ++r) st1(const_cast<float *>(s.p[r]) + i, acc);
     } else {
-        table_scalar_body<MODE>(p, src);
+        st1(p.out + i, acc);
     }
 }
 
+template <int WT, int MODE>
+__device__ __noinline__ void table_small_edges(const TableParams &p, SrcSet<WT> s, int i, int head, int tail0)
+{
+    if (i < head) table_fold_one<WT, MODE>(p, s, i);
+    if (i < (int)p.len - tail0) table_fold_one<WT, MODE>(p, s, tail0 + i);
+}
+
+// A small call whose entries share no 32-byte phase: 16-byte vectors if
+// they share a 16-byte phase, else scalars.
+template <int WT, int MODE>
+__device__ __noinline__ void table_small_slow(const TableParams &p, SrcSet<WT> s, bool same4)
+{
+    if (same4) {
+        const int64_t head = (4 - phase_of(s.p[0], 4)) % 4;
+        table_fixed_vec<WT, 4, MODE>(p, s.p, head > p.len ? p.len : head);
+    } else {
+        table_scalar_body<MODE>(p, s.p);
+    }
+}
+
+// Small payloads (len <= DETFOLD_SMALL_LEN) with W <= 8. Every thread reads
+// the (broadcast) table entries into registers and checks them itself, with
+// no shared memory and no block barrier between the table load and the data
+// loads. The common case, every entry (and the output) at one 32-byte phase,
+// is one 32-byte vector per thread with 32-bit indices; the head and tail
+// and the narrower widths run out of line, so the code a CTA executes after
+// the wait -- what the latency of a graph of small folds is made of -- stays
+// short.
+template <int WT, int MODE>
+__global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) fold_table_small_kernel(const __grid_constant__ TableParams p)
+{
+    static_assert(DETFOLD_SMALL_LEN < (1 << 30), "small-path indices are 32-bit");
+    pdl_enter(p.pdl);
+    SrcSet<WT> s;
+#pragma unroll
+    for (int r = 0; r < WT; ++r) s.p[r] = p.table[r];
+    int code = DETFOLD_OK;
+#pragma unroll
+    for (int r = 0; r < WT; ++r) {
+        if (code == DETFOLD_OK && s.p[r] == nullptr) code = DETFOLD_ERR_NULL;
+        if (code == DETFOLD_OK && ((uintptr_t)s.p[r] & 3u)) code = DETFOLD_ERR_ALIGN;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.status) *p.status = code;
+    if (code != DETFOLD_OK) return;
+    // byte phase within 32 bytes; every pointer is 4-byte aligned here
+    const unsigned ph0 = (unsigned)(uintptr_t)s.p[0] & 31u;
+    unsigned diff = (MODE == kAllReduce) ? 0u : (((unsigned)(uintptr_t)p.out & 31u) ^ ph0);
+#pragma unroll
+    for (int r = 1; r < WT; ++r) diff |= ((unsigned)(uintptr_t)s.p[r] & 31u) ^ ph0;
+    if (diff != 0) {
+        table_small_slow<WT, MODE>(p, s, (diff & 15u) == 0);
+        return;
+    }
+    const int len = (int)p.len;
+    int head = (int)(((32u - ph0) & 31u) / 4);
+    if (head > len) head = len;
+    const int nvec = (len - head) / 8;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < nvec) {
+        const int e = head + i * 8;
+        Vec<8> x[WT];
+#pragma unroll
+        for (int r = 0; r < WT; ++r) x[r] = ldv<8, false>(s.p[r] + e);
+        Vec<8> acc = x[0];
+#pragma unroll
+        for (int r = 1; r < WT; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc.v[j] = __fadd_rn(acc.v[j], x[r].v[j]);
+        if (p.do_scale) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc.v[j] = __fmul_rn(acc.v[j], p.scale);
+        }
+        if constexpr (MODE == kAllReduce) {
+#pragma unroll
+            for (int r = 0; r < WT; ++r) stv<8>(const_cast<float *>(s.p[r]) + e, acc);
+        } else {
+            stv<8>(p.out + e, acc);
+        }
+    }
+    const int tail0 = head + nvec * 8;
+    if ((head != 0 || tail0 != len) && i < 8) table_small_edges<WT, MODE>(p, s, i, head, tail0);
+}
+
 template <int WT>
-cudaError_t launch_table_fixed(const TableParams &p, int64_t work, bool small, int mode,
-                               cudaStream_t stream)
+cudaError_t launch_table_small(const TableParams &p, int64_t work, int mode, cudaStream_t stream)
 {
     if (mode == kAllReduce)
-        return launch_kernel<fold_table_fixed_kernel<WT, kAllReduce>>(p, work, 1, small, 256, 0, stream);
-    return launch_kernel<fold_table_fixed_kernel<WT, kSumCoherent>>(p, work, 1, small, 256, 0, stream);
+        return launch_kernel<fold_table_small_kernel<WT, kAllReduce>>(p, work, 1, true, 256, 0, stream);
+    return launch_kernel<fold_table_small_kernel<WT, kSumCoherent>>(p, work, 1, true, 256, 0, stream);
 }
 
 }  // namespace
@@ -269,17 +338,18 @@ cudaError_t launch_table(const float *const *d_table, float *out, int *d_status,
     const bool small = len <= DETFOLD_SMALL_LEN;
     p.pdl = ((small && DETFOLD_SMALL_PDL) || DETFOLD_PDL_ALL) ? 1 : 0;
     const int64_t work = (len + 7) / 8 > 0 ? (len + 7) / 8 : 1;  // vectors if 32-byte access
-    // Small payloads: the register-table kernel (shortest dependent chain).
-    // Bandwidth-sized calls: the shared-memory table kernel (fewer registers).
+    // Small payloads: the register-table kernel (shortest dependent chain;
+    // one thread per 32-byte vector). Bandwidth-sized calls: the
+    // shared-memory table kernel (fewer registers).
     switch (small ? W : 0) {
-    case 1: return launch_table_fixed<1>(p, work, small, mode, stream);
-    case 2: return launch_table_fixed<2>(p, work, small, mode, stream);
-    case 3: return launch_table_fixed<3>(p, work, small, mode, stream);
-    case 4: return launch_table_fixed<4>(p, work, small, mode, stream);
-    case 5: return launch_table_fixed<5>(p, work, small, mode, stream);
-    case 6: return launch_table_fixed<6>(p, work, small, mode, stream);
-    case 7: return launch_table_fixed<7>(p, work, small, mode, stream);
-    case 8: return launch_table_fixed<8>(p, work, small, mode, stream);
+    case 1: return launch_table_small<1>(p, work, mode, stream);
+    case 2: return launch_table_small<2>(p, work, mode, stream);
+    case 3: return launch_table_small<3>(p, work, mode, stream);
+    case 4: return launch_table_small<4>(p, work, mode, stream);
+    case 5: return launch_table_small<5>(p, work, mode, stream);
+    case 6: return launch_table_small<6>(p, work, mode, stream);
+    case 7: return launch_table_small<7>(p, work, mode, stream);
+    case 8: return launch_table_small<8>(p, work, mode, stream);
     default: break;
     }
     if (mode == kAllReduce)

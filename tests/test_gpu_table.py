@@ -41,6 +41,48 @@ def test_table_fold_matches_oracle(W, n, phases):
     assert out.intact() and all(s.intact() for s in srcs)
 
 
+# per-rank element offsets -> the access width the kernel must pick
+PHASE_PLANS = {
+    "32B+head": lambda r: 5,            # one 32-byte phase, head 3
+    "16B": lambda r: 4 * (r % 2),       # 16-byte phase shared, 32-byte phase not
+    "16B+head": lambda r: 1 + 4 * (r % 2),
+    "scalar": lambda r: r % 4,
+}
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+@pytest.mark.parametrize("n", [1, 9, 1034, 4099, 65536 + 3, 1 << 17, (1 << 17) + 1])
+@pytest.mark.parametrize("plan", sorted(PHASE_PLANS))
+def test_table_access_widths_heads_and_tails(W, n, plan):
+    # The table kernels choose the access width on the device from the
+    # entries' phases; every width, with heads and tails, on both sides of
+    # the small-payload bound (2^17 elements), for the sum, the in-place sum
+    # and the all-reduce.
+    rows = gen.stress_rows(W, n)
+    offs = [PHASE_PLANS[plan](r) for r in range(W)]
+    srcs = [Guarded(n, offs[r], rows[r]) for r in range(W)]
+    out = Guarded(n, offs[0])
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    df.detfold_sum_ptrs_dev(out.t, df.device_table([t.t for t in srcs]), W, n, status)
+    sync()
+    assert int(status.item()) == 0
+    want = oracle.fold(rows)
+    assert_bitwise(out.host(), want, f"table fold W={W} n={n} {plan}")
+    assert out.intact() and all(t.intact() for t in srcs)
+    df.detfold_sum_ptrs_dev(srcs[0].t, df.device_table([t.t for t in srcs]), W, n)
+    sync()
+    assert_bitwise(srcs[0].host(), want, f"table in-place W={W} n={n} {plan}")
+    scale = float(oracle.mean_scale(W))
+    arenas = [Guarded(n, offs[r], rows[r]) for r in range(W)]
+    df.detfold_loopback_allreduce_dev(df.device_table([a.t for a in arenas]), W, n, scale)
+    sync()
+    exp = [rows[r].copy() for r in range(W)]
+    oracle.allreduce(exp, np.float32(scale))
+    for r in range(W):
+        assert_bitwise(arenas[r].host(), exp[r], f"table all-reduce W={W} n={n} {plan} rank={r}")
+        assert arenas[r].intact()
+
+
 @pytest.mark.parametrize("W", [2, 3, 4, 6])
 @pytest.mark.parametrize("n", [5, 65536 + 3, (1 << 20) + 7])
 def test_table_allreduce_and_in_place_fold(W, n):

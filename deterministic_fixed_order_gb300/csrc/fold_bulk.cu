@@ -20,9 +20,10 @@
 // says so.
 //
 // Preconditions, checked by the dispatcher: W <= 8, every operand at the same
-// 32-byte phase (tiles then start 32-byte aligned), at least one whole tile.
-// The head before the first tile and the tail after the last are folded by
-// scalar code in the same launch.
+// 16-byte phase (tiles then start 16-byte aligned), at least one whole tile.
+// The head before the first tile (scalar) and the tail after the last (16-byte
+// vectors spread over the CTAs that hold the fewest tiles) are folded in the
+// same launch.
 #include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -74,6 +75,58 @@ struct BulkParams {
     int pdl;
 };
 
+// The elements outside the whole tiles: the head [0, head), fewer than 8, and
+// the tail [head + ntiles*T, len), fewer than T. The tail starts where a tile
+// would, 16-byte aligned: its whole 16-byte vectors go one per consumer
+// thread, starting from the last CTA (the CTAs at the end hold the fewest
+// tiles); the head and the tail's last few (fewer than 4) elements are
+// scalar, in the last CTA. Consumers do this before their tiles, while the
+// producer's first loads are in flight.
+template <int W, int MODE>
+__device__ __forceinline__ void bulk_edges(const BulkParams<W> &p, int tc)
+{
+    constexpr int T = BulkShape<W>::T, NC = 32 * BulkShape<W>::NCW;
+    const int64_t tail0 = p.head + p.ntiles * T;
+    const int64_t nv = (p.len - tail0) / 4;
+    for (int64_t v = (int64_t)(gridDim.x - 1 - blockIdx.x) * NC + tc; v < nv; v += (int64_t)gridDim.x * NC) {
+        const int64_t e = tail0 + v * 4;
+        Vec<4> x[W];
+#pragma unroll
+        for (int r = 0; r < W; ++r) x[r] = ldv<4, false>(p.a[r] + e);
+        Vec<4> acc = x[0];
+#pragma unroll
+        for (int r = 1; r < W; ++r)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc.v[k] = __fadd_rn(acc.v[k], x[r].v[k]);
+        if (p.do_scale) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc.v[k] = __fmul_rn(acc.v[k], p.scale);
+        }
+        if constexpr (MODE == kAllReduce) {
+#pragma unroll
+            for (int r = 0; r < W; ++r) stv<4>(p.a[r] + e, acc);
+        } else {
+            stv<4>(p.out + e, acc);
+        }
+    }
+    if (blockIdx.x != gridDim.x - 1) return;
+    const int64_t rest0 = tail0 + nv * 4;
+    const int nhead = (int)p.head, nrest = (int)(p.len - rest0);
+    if (tc < nhead + nrest) {
+        const int64_t i = tc < nhead ? tc : rest0 + (tc - nhead);
+        float acc = ld1<false>(p.a[0] + i);
+#pragma unroll
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<false>(p.a[r] + i));
+        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+        if constexpr (MODE == kAllReduce) {
+#pragma unroll
+            for (int r = 0; r < W; ++r) st1(p.a[r] + i, acc);
+        } else {
+            st1(p.out + i, acc);
+        }
+    }
+}
+
 template <int W, int MODE>
 __global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const __grid_constant__ BulkParams<W> p)
 {
@@ -113,6 +166,7 @@ __global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const 
     }
 
     const int tc = threadIdx.x - 32;
+    bulk_edges<W, MODE>(p, tc);
     long long k = 0;
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
         const int s = (int)(k % S);
@@ -154,25 +208,6 @@ __global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const 
         }
     }
     if (tc == 0) bulk_wait_all();
-
-    // head [0, head) and tail [head + ntiles*T, len): scalar, by the last CTA
-    if (blockIdx.x == gridDim.x - 1) {
-        const int64_t tail0 = p.head + p.ntiles * T;
-        const int64_t nhead = p.head, ntail = p.len - tail0;
-        for (int64_t q = tc; q < nhead + ntail; q += NC) {
-            const int64_t i = q < nhead ? q : tail0 + (q - nhead);
-            float acc = ld1<false>(p.a[0] + i);
-#pragma unroll
-            for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<false>(p.a[r] + i));
-            if (p.do_scale) acc = __fmul_rn(acc, p.scale);
-            if constexpr (MODE == kAllReduce) {
-#pragma unroll
-                for (int r = 0; r < W; ++r) st1(p.a[r] + i, acc);
-            } else {
-                st1(p.out + i, acc);
-            }
-        }
-    }
 }
 
 // Shared-memory opt-in and resident CTAs, once per kernel and device.

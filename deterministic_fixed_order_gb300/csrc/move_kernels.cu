@@ -95,13 +95,27 @@ __global__ void __launch_bounds__(64) move_bulk_kernel(const __grid_constant__ M
             }
         }
         bulk_wait_all();
-    } else if (threadIdx.x > 32 && blockIdx.x == gridDim.x - 1) {
-        // head [0, head) and tail [head + ntiles*T, len), scalar, by 31 lanes
+    } else {
+        // The 62 other threads move what lies outside the whole tiles: the
+        // tail [head + ntiles*T, len) starts 16-byte aligned and goes in
+        // 16-byte vectors, one per thread, from the last CTA (the CTAs at the
+        // end hold the fewest tiles); the head [0, head) and the tail's last
+        // few elements (fewer than 4 each) are scalar, in the last CTA.
+        constexpr int NE = 62;
+        const int et = threadIdx.x < 32 ? threadIdx.x - 1 : threadIdx.x - 2;
         const int64_t tail0 = p.head + p.ntiles * T;
-        const int64_t nhead = p.head, ntail = p.len - tail0;
-        for (int64_t q = threadIdx.x - 33; q < nhead + ntail; q += 31) {
-            const int64_t i = q < nhead ? q : tail0 + (q - nhead);
-            for (int k = 0; k < p.K; ++k) st1(p.dst[k] + i, ld1<true>(p.src[p.grp[k]] + i));
+        const int64_t nv = (p.len - tail0) / 4;
+        for (int64_t v = (int64_t)(gridDim.x - 1 - blockIdx.x) * NE + et; v < nv; v += (int64_t)gridDim.x * NE) {
+            const int64_t e = tail0 + v * 4;
+            for (int k = 0; k < p.K; ++k) stv<4>(p.dst[k] + e, ldv<4, true>(p.src[p.grp[k]] + e));
+        }
+        if (blockIdx.x == gridDim.x - 1) {
+            const int64_t rest0 = tail0 + nv * 4;
+            const int nhead = (int)p.head, nrest = (int)(p.len - rest0);
+            if (et < nhead + nrest) {
+                const int64_t i = et < nhead ? et : rest0 + (et - nhead);
+                for (int k = 0; k < p.K; ++k) st1(p.dst[k] + i, ld1<true>(p.src[p.grp[k]] + i));
+            }
         }
     }
 }

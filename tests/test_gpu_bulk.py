@@ -81,9 +81,11 @@ def _bits_rows(W, n, seed):
         .astype(np.uint32).view(np.float32)
 
 
-@pytest.mark.parametrize("n", [M, M + 5, 3 * M + 2049])
+@pytest.mark.parametrize("n", [M, M + 5, M + 2047, M + 2053, 3 * M + 2049])
 @pytest.mark.parametrize("nd", [1, 3, 7])
 def test_bulk_broadcast_moves_bytes_exactly(n, nd):
+    # offset 2: a 2-element head; M + 2047 and M + 2053 leave tails of 2045
+    # and 3 elements after the 8 KB tiles (16-byte vectors, then scalars)
     src_h = _bits_rows(1, n, n + nd)[0]
     src = Guarded(n, 2, src_h)
     dsts = [Guarded(n, 2) for _ in range(nd)]
@@ -106,8 +108,9 @@ def test_bulk_all_gather_and_staged(W):
     for r, o in enumerate(outs):
         assert_bitwise(o.host(), want, f"bulk all-gather W={W} rank={r}")
         assert o.intact()
-    # the staged comparator with shards of at least 2^20: bulk exchange and distribute
-    n = W * M + 13
+    # the staged comparator with shards of at least 2^20: bulk exchange and
+    # distribute, with shard tails of about 2000 elements after the tiles
+    n = W * (M + 2000) + 13
     rows = gen.normal_rows(W, n)
     arenas = [Guarded(n, 1, rows[r]) for r in range(W)]
     nb = df.detfold_staged_workspace_bytes(n, W)

@@ -335,7 +335,28 @@ int detfold_all_gather(float *const *outs, int W, const float *const *parts, int
     for (int r = 0; r < W; ++r)
         for (int p = 0; p < W; ++p)
             if (intersects(outs[r], total * 4, parts[p], span * 4)) return DETFOLD_ERR_OVERLAP;
-    // Part p lands at offset p*span of every output: one broadcast per part.
+    // Part p lands at offset p*span of every output. With at most 8 parts and
+    // every pair at one 16-byte phase, all W*W pairs go in one launch, ordered
+    // by part (the bulk movement path reads each part once and stores it W
+    // times); otherwise one broadcast per part.
+    if (W <= 8) {
+        const uintptr_t ph = (uintptr_t)parts[0] & 15u;
+        bool same = true;
+        for (int p = 0; same && p < W; ++p) {
+            same = ((uintptr_t)parts[p] & 15u) == ph;
+            for (int r = 0; same && r < W; ++r) same = ((uintptr_t)(outs[r] + (int64_t)p * span) & 15u) == ph;
+        }
+        if (same) {
+            const float *from[64];
+            float *to[64];
+            for (int p = 0; p < W; ++p)
+                for (int r = 0; r < W; ++r) {
+                    from[p * W + r] = parts[p];
+                    to[p * W + r] = outs[r] + (int64_t)p * span;
+                }
+            return cuda_status(detfold::launch_move(from, to, W * W, span, (cudaStream_t)stream));
+        }
+    }
     for (int p = 0; p < W; ++p) {
         const float *from[DETFOLD_MAX_W];
         float *to[DETFOLD_MAX_W];

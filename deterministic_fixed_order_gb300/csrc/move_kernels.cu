@@ -209,6 +209,36 @@ __global__ void __launch_bounds__(256) move_pairs_kernel(const __grid_constant__
     }
 }
 
+// The head and tail elements of a small move (fewer than VEC each per pair),
+// out of line: thread i < K * (head + tail) moves one element of one pair.
+__device__ __noinline__ void move_small_edges(const MoveParams &p, int i, int nedge, int tail0)
+{
+    const int k = i / nedge, q = i - k * nedge;
+    const int e = q < (int)p.head ? q : tail0 + (q - (int)p.head);
+    st1(p.dst[k] + e, ld1<true>(p.src[k] + e));
+}
+
+// Small moves (len <= DETFOLD_SMALL_LEN, every pointer at one phase): one
+// (pair, vector) per thread with 32-bit indices, so a call is one dependent
+// load and store, not one per group of pairs as in the looping kernel above.
+// Pairs that share a source load it separately (from L2, at these sizes).
+template <int VEC>
+__global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) move_small_kernel(const __grid_constant__ MoveParams p)
+{
+    static_assert((int64_t)DETFOLD_SMALL_LEN * kMaxPairs < (1LL << 31), "small-move indices are 32-bit");
+    pdl_enter(p.pdl);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int nvec = (int)p.nvec;
+    if (i < p.K * nvec) {
+        const int k = i / nvec;
+        const int e = (int)p.head + (i - k * nvec) * VEC;
+        stv<VEC>(p.dst[k] + e, ldv<VEC, true>(p.src[k] + e));
+    }
+    const int tail0 = (int)p.head + nvec * VEC;
+    const int nedge = (int)p.len - nvec * VEC;  // head + tail
+    if (nedge > 0 && i < p.K * nedge) move_small_edges(p, i, nedge, tail0);
+}
+
 // Operands at different 4-byte phases: coalesced scalar moves.
 __global__ void __launch_bounds__(256) move_pairs_scalar_kernel(const __grid_constant__ MoveParams p)
 {
@@ -275,6 +305,14 @@ static cudaError_t launch_move_chunk(const float *const *src, float *const *dst,
             p.nvec = (len - head) / cand;
             break;
         }
+    }
+    if (small && vec != 0) {
+        // one thread per (pair, vector), and enough threads for the edges
+        int64_t work = (int64_t)K * p.nvec;
+        const int64_t edges = (int64_t)K * (len - p.nvec * vec);
+        if (edges > work) work = edges;
+        if (vec == 8) return launch_kernel<move_small_kernel<8>>(p, work, 1, true, 256, 0, stream);
+        return launch_kernel<move_small_kernel<4>>(p, work, 1, true, 256, 0, stream);
     }
     if (vec == 8) return launch_kernel<move_pairs_kernel<8>>(p, p.nvec, 1, small, 256, 0, stream);
     if (vec == 4) return launch_kernel<move_pairs_kernel<4>>(p, p.nvec, 1, small, 256, 0, stream);

@@ -321,6 +321,32 @@ def test_broadcast_and_all_gather_move_bytes_exactly(span, W):
         assert o.intact()
 
 
+@pytest.mark.parametrize("span", [1, 7, 1024, 4099, 16384, 1 << 17, (1 << 17) + 1])
+@pytest.mark.parametrize("W", [2, 3, 8])
+@pytest.mark.parametrize("off", [0, 1, 4, 7])
+def test_movement_at_one_phase_with_heads_and_tails(span, W, off):
+    # Every pointer at one phase: the vector movement kernels, with a head and
+    # a tail at offsets 1 and 7; spans up to 2^17 take the small-move kernel
+    # (one pair-vector per thread), 2^17 + 1 the looping kernel.
+    src_h = _random_bits(span, 57 + span)
+    src = Guarded(span, off, src_h)
+    dsts = [Guarded(span, off) for _ in range(W - 1)]
+    df.detfold_broadcast([d.t for d in dsts], W - 1, src.t, span)
+    sync()
+    for k, d in enumerate(dsts):
+        assert d.intact()
+        assert_bitwise(d.host(), src_h, f"broadcast span={span} off={off} dst={k}")
+    parts_h = [_random_bits(span, 67 + r + span) for r in range(W)]
+    parts = [Guarded(span, off, parts_h[r]) for r in range(W)]
+    outs = [Guarded(W * span, off) for _ in range(W)]
+    df.detfold_all_gather([o.t for o in outs], W, [p.t for p in parts], span)
+    sync()
+    want = np.concatenate(parts_h)
+    for r, o in enumerate(outs):
+        assert o.intact()
+        assert_bitwise(o.host(), want, f"all-gather span={span} off={off} rank={r}")
+
+
 def test_broadcast_many_destinations_splits_launches():
     # more destinations than one parameter block holds
     span, nd = 1000, 256

@@ -459,54 +459,107 @@ def copy_peak_gbs(torch, dev) -> float:
     return best
 
 
-def cpu_baseline(oracle, gen, budget_s: float = 12.0) -> dict:
-    """The oracle as it stands, single-threaded, on a bounded sample of every
-    row of the step: the first S elements of each rank's arena (S = 2^21 for
-    the large rows, the full length for the small ones), repeated until the
-    budget is spent."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+        if m:
+            return m.group(1).strip()
+        part = re.search(r"^CPU part\s*:\s*(\S+)$", info, re.M)
+        impl = re.search(r"^CPU implementer\s*:\s*(\S+)$", info, re.M)
+        if part and impl:
+            return f"implementer {impl.group(1)}, part {part.group(1)}"
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(oracle, gen, budget_s: float = 12.0, split_budget_s: float = 4.0) -> dict:
+    """The oracle as it stands on a bounded sample of every row of the step:
+    the first S elements of each rank's arena (S = 2^21 for the large rows,
+    the full length for the small ones), repeated until the budget is spent.
+    `value` is single-threaded. `threads_split` is the same per-element chains
+    with every row's elements split into one contiguous range per host core,
+    each range folded by the same oracle call on its own thread (the oracle's
+    C calls release the GIL); the chain of every element is unchanged."""
     S = 1 << 21
-    sample_bytes = 0
-    parts = []
     c3 = gen.gradient_rows(C3_W, S)
     c4 = gen.normal_rows(C4_W, S)
     c5 = {W: gen.stress_rows(W, C5_N) for W in C5_WS}
     c2 = {n: gen.c1_rows(2, n) for n in C2_NS}
     s4 = np.float32(0.25)
+    pass_bytes = (2 * (C3_W + 1) * S * 4 + 2 * (2 * C4_W * S * 4)
+                  + sum(((W + 1) + 2 + 2 * W) * C5_N * 4 for W in C5_WS)
+                  + sum(3 * n * 4 for n in C2_NS))
 
-    def one_pass():
-        nonlocal sample_bytes
-        oracle.fold_stacked(c3)
-        oracle.fold(c3)
-        sample_bytes_local = 2 * (C3_W + 1) * S * 4
-        a = [c4[r].copy() for r in range(C4_W)]
+    def one_pass(lo: float = 0.0, hi: float = 1.0, stacked: bool = True):
+        def cols(n):
+            return int(n * lo), int(n * hi)
+        a3, b3 = cols(S)
+        rows3 = [c3[r, a3:b3] for r in range(C3_W)]
+        if stacked:
+            oracle.fold_stacked(c3)
+        else:
+            oracle.fold(rows3)  # a column range of a stack is not contiguous
+        oracle.fold(rows3)
+        a = [c4[r, a3:b3].copy() for r in range(C4_W)]
         oracle.allreduce(a, s4)
-        a = [c4[r].copy() for r in range(C4_W)]
+        a = [c4[r, a3:b3].copy() for r in range(C4_W)]
         oracle.staged_allreduce(a, s4)
-        sample_bytes_local += 2 * (2 * C4_W * S * 4)
+        a5, b5 = cols(C5_N)
         for W in C5_WS:
             m = oracle.mean_scale(W)
-            oracle.scale(oracle.fold(c5[W]), m)
-            a = [c5[W][r].copy() for r in range(W)]
+            oracle.scale(oracle.fold([c5[W][r, a5:b5] for r in range(W)]), m)
+            a = [c5[W][r, a5:b5].copy() for r in range(W)]
             oracle.allreduce(a, m)
-            sample_bytes_local += ((W + 1) + 2 + 2 * W) * C5_N * 4
         for n in C2_NS:
-            oracle.fold_stacked(c2[n])
-            sample_bytes_local += 3 * n * 4
-        return sample_bytes_local
+            a2, b2 = cols(n)
+            if a2 < b2:
+                oracle.fold([c2[n][r, a2:b2] for r in range(2)])
 
     t0 = time.perf_counter()
-    total = 0
     passes = 0
     while True:
-        total += one_pass()
+        one_pass()
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": total / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    value = passes * pass_bytes / el / 1e9
+
+    from concurrent.futures import ThreadPoolExecutor
+    T = os.cpu_count() or 1
+    with ThreadPoolExecutor(max_workers=T) as ex:
+        def split_pass():
+            list(ex.map(lambda k: one_pass(k / T, (k + 1) / T, stacked=False), range(T)))
+        split_pass()  # warm the pool
+        t0 = time.perf_counter()
+        split_passes = 0
+        while True:
+            split_pass()
+            split_passes += 1
+            el_split = time.perf_counter() - t0
+            if el_split >= split_budget_s:
+                break
+    return {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{passes} passes over the first 2^21 elements of every C3/C4 rank row "
                       f"and the full C5/C2 rows (all rows of one step), {el:.1f} s, "
-                      f"single-threaded serial fold"}
+                      f"single-threaded serial fold",
+            "cpu_model": cpu_model(),
+            "threads_split": {"value": round(split_passes * pass_bytes / el_split / 1e9, 3), "unit": "GB/s",
+                              "cores": T,
+                              "sample": f"the same sample, {split_passes} passes in {el_split:.1f} s, "
+                                        f"every row's elements split into {T} contiguous ranges, "
+                                        f"one thread each"}}
 
 
 def run_gpu(args) -> None:

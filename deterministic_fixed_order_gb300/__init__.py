@@ -108,36 +108,78 @@ def _check(status: int, where: str) -> None:
         raise DetfoldError(status, where)
 
 
-def _dev_ptr(x, need_elems: int | None, what: str) -> int:
-    """Address of a device operand; tensors are checked against need_elems."""
+_torch = None          # torch, imported on first use
+_F32 = None
+_cuda_ok = None        # torch.cuda.is_available(), asked once
+_raw_stream = None     # torch's raw current-stream query, if this torch has it
+_ARRAYS = {}           # ctypes pointer-array types by length
+
+
+def _t():
+    global _torch, _F32
+    if _torch is None:
+        import torch
+        _torch, _F32 = torch, torch.float32
+    return _torch
+
+
+def _label(what: str, k) -> str:
+    return what if k is None else f"{what}[{k}]"
+
+
+def _dev_ptr(x, need_elems: int | None, what: str, k=None) -> int:
+    """Address of a device operand; tensors are checked against need_elems.
+    (The checks run on every call; the messages are built only on failure.)"""
     if x is None:
         return 0
     if isinstance(x, int):
         return x
-    import torch
+    torch = _torch or _t()
     if not isinstance(x, torch.Tensor):
-        raise TypeError(f"{what}: expected a CUDA float32 tensor or an int address")
-    if not x.is_cuda or x.dtype != torch.float32:
-        raise TypeError(f"{what}: expected a CUDA float32 tensor, got {x.device} {x.dtype}")
+        raise TypeError(f"{_label(what, k)}: expected a CUDA float32 tensor or an int address")
+    if not x.is_cuda or x.dtype is not _F32:
+        raise TypeError(f"{_label(what, k)}: expected a CUDA float32 tensor, got {x.device} {x.dtype}")
     if not x.is_contiguous():
-        raise ValueError(f"{what}: tensor must be contiguous")
+        raise ValueError(f"{_label(what, k)}: tensor must be contiguous")
     if need_elems is not None and x.numel() < need_elems:
-        raise ValueError(f"{what}: tensor holds {x.numel()} elements, call needs {need_elems}")
+        raise ValueError(f"{_label(what, k)}: tensor holds {x.numel()} elements, call needs {need_elems}")
     return x.data_ptr()
+
+
+def _current_stream() -> int:
+    """Handle of torch's current stream on the current device (0 without CUDA).
+    After the first call initializes torch's CUDA state through the public
+    API, the handle comes from torch's raw stream query, which skips building
+    a Stream object."""
+    global _cuda_ok, _raw_stream
+    if _cuda_ok is None:
+        torch = _t()
+        _cuda_ok = torch.cuda.is_available()
+        if _cuda_ok:
+            torch.cuda.init()
+            _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if not _cuda_ok:
+        return 0
+    if _raw_stream is not None:
+        return _raw_stream(_torch._C._cuda_getDevice())
+    return _torch.cuda.current_stream().cuda_stream
 
 
 def _stream(s) -> int:
     if s is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+        return _current_stream()
     if isinstance(s, int):
         return s
     return s.cuda_stream
 
 
 def _ptr_array(items, need_elems, what):
-    ptrs = [_dev_ptr(t, need_elems, f"{what}[{k}]") for k, t in enumerate(items)]
-    return (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
+    ptrs = [_dev_ptr(t, need_elems, what, k) for k, t in enumerate(items)]
+    n = max(1, len(ptrs))
+    arr = _ARRAYS.get(n)
+    if arr is None:
+        arr = _ARRAYS.setdefault(n, ctypes.c_void_p * n)
+    return arr(*ptrs)
 
 
 # ------------------------------------------------------------------ status-returning calls
@@ -168,7 +210,7 @@ def status_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: fl
     tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
     ws = workspace
     if ws is not None and not isinstance(ws, int):
-        import torch
+        torch = _torch or _t()
         if not ws.is_cuda or not ws.is_contiguous():
             raise ValueError("workspace: expected a contiguous CUDA tensor")
         if ws.numel() * ws.element_size() < workspace_bytes:
@@ -200,7 +242,7 @@ def _table_ptr(table, W: int) -> int:
     """Address of a device pointer table: a CUDA int64 tensor of >= W entries, or an int."""
     if isinstance(table, int):
         return table
-    import torch
+    torch = _torch or _t()
     if not isinstance(table, torch.Tensor) or not table.is_cuda or table.dtype != torch.int64:
         raise TypeError("table: expected a CUDA int64 tensor of device addresses")
     if not table.is_contiguous() or table.numel() < W:
@@ -211,7 +253,7 @@ def _table_ptr(table, W: int) -> int:
 def _status_ptr(status) -> int:
     if status is None or isinstance(status, int):
         return status or 0
-    import torch
+    torch = _torch or _t()
     if not status.is_cuda or status.dtype != torch.int32 or status.numel() < 1:
         raise TypeError("status: expected a CUDA int32 tensor")
     return status.data_ptr()
@@ -220,7 +262,7 @@ def _status_ptr(status) -> int:
 def device_table(tensors, device=None):
     """A CUDA int64 tensor holding the data addresses of `tensors` (for the
     *_dev entry points). Each tensor must be a CUDA float32 tensor."""
-    import torch
+    torch = _torch or _t()
     ptrs = [_dev_ptr(t, None, f"tensors[{k}]") for k, t in enumerate(tensors)]
     dev = device if device is not None else tensors[0].device
     return torch.tensor(ptrs, dtype=torch.int64, device=dev)
@@ -241,7 +283,7 @@ def _raw_dev(x, nbytes: int, what: str) -> int:
     """Address of a CUDA tensor of at least nbytes (any dtype), or an int."""
     if isinstance(x, int):
         return x
-    import torch
+    torch = _torch or _t()
     if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous():
         raise TypeError(f"{what}: expected a contiguous CUDA tensor")
     if x.numel() * x.element_size() < nbytes:
@@ -333,7 +375,7 @@ class OneShotLink:
     refusal words, and the host-side epoch, which grows by one per call."""
 
     def __init__(self, W: int, max_len: int, device="cuda"):
-        import torch
+        torch = _torch or _t()
         self.W, self.max_len = W, max_len
         self.link = torch.zeros(DETFOLD_ONESHOT_LINK_BYTES // 8, dtype=torch.int64, device=device)
         self.stage = torch.empty(max(1, W * max_len), dtype=torch.float32, device=device)
@@ -402,7 +444,7 @@ def detfold_memory_floor(src, dst, count: int, pdl: int = 1, stream=None) -> Non
 
 def sum_stacked(stacked, out=None, stream=None):
     """out = fold of the rows of a [W, len] CUDA float32 tensor."""
-    import torch
+    torch = _torch or _t()
     W, n = stacked.shape
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=stacked.device)
@@ -411,7 +453,7 @@ def sum_stacked(stacked, out=None, stream=None):
 
 
 def sum_ptrs(srcs, out=None, stream=None):
-    import torch
+    torch = _torch or _t()
     n = srcs[0].numel()
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=srcs[0].device)

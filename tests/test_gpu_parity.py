@@ -543,3 +543,26 @@ def test_floor_probes(pdl):
     sync()
     assert dst.intact()
     assert_bitwise(dst.host(), np.arange(1, 33, dtype=np.float32), "memory floor copy in a graph")
+
+
+def test_binding_enqueues_on_torchs_current_stream():
+    # the binding's fast query of torch's current stream agrees with torch's
+    # public one, inside and outside a stream context, and in another thread
+    assert df._stream(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert df._stream(None) == s.cuda_stream == torch.cuda.current_stream().cuda_stream
+    assert df._stream(None) == torch.cuda.current_stream().cuda_stream
+    import threading
+    seen = []
+
+    def other():
+        t = torch.cuda.Stream()
+        with torch.cuda.stream(t):
+            seen.append(df._stream(None) == t.cuda_stream)
+        seen.append(df._stream(None) == torch.cuda.current_stream().cuda_stream)
+
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen == [True, True]

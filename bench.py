@@ -421,15 +421,39 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
         return statistics.median(ts)
     for _ in range(5):
         link.all_reduce(arenas)
+    torch.cuda.synchronize()
 
     def one_shot():
-        link.epoch += 1
-        df.detfold_one_shot_allreduce(arenas, 2, n, 1.0, link.link, link.epoch, link.stage,
-                                      link.words)
+        df.detfold_one_shot_allreduce(arenas, 2, n, 1.0, link.link, 0, link.stage, link.words)
     out["one_shot_W2_16KiB_us_per_call"] = round(per_call_us(one_shot), 2)
     out["one_shot_barrier_errors"] = link.barrier_errors()
     out["fused_W2_16KiB_us_per_call_same_timing"] = round(
         per_call_us(lambda: df.detfold_loopback_allreduce(arenas, 2, n, 1.0)), 2)
+    # the same two calls back to back in CUDA graphs of 1000 nodes (the
+    # one-shot takes each node's epoch from the link's counter)
+    gs = torch.cuda.Stream()
+    for key, fn in (("one_shot_W2_16KiB_graph_us_per_call", one_shot),
+                    ("fused_W2_16KiB_graph_us_per_call",
+                     lambda: df.detfold_loopback_allreduce(arenas, 2, n, 1.0))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            for _ in range(1000):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(7):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(gs):
+                a.record()
+                g.replay()
+                b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[key] = round(statistics.median(ts), 3)  # ms per 1000 calls = us per call
+        del g
+    out["one_shot_barrier_errors_after_graphs"] = link.barrier_errors()
     # mismatched phases at the C3 size: the rows of an [8][2^26 - 3] stack sit
     # at eight different 4-byte phases, so the realigned kernel runs
     nm = C3_N - 3

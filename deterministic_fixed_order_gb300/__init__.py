@@ -47,7 +47,8 @@ STATUS = {
 DETFOLD_NOALLOC_SCRATCH_BYTES = 16 << 20
 DETFOLD_ONESHOT_MAX_W = 64
 DETFOLD_ONESHOT_MAX_LEN = 1 << 22
-DETFOLD_ONESHOT_LINK_BYTES = 2 * 1024 * 8
+DETFOLD_ONESHOT_MAX_CTAS = 1024
+DETFOLD_ONESHOT_LINK_BYTES = 2 * DETFOLD_ONESHOT_MAX_CTAS * 8 + 64
 DETFOLD_ONESHOT_REFUSE_ENTRY = 40043
 DETFOLD_ONESHOT_REFUSE_EXIT = 40044
 
@@ -371,8 +372,8 @@ def detfold_one_shot_allreduce(arenas, W: int, length: int, mean_scale: float, l
 
 class OneShotLink:
     """Device state of one emulated one-shot link between W ranks: barrier
-    flags (zero-filled once), W stage rows of up to max_len floats, the W
-    refusal words, and the host-side epoch, which grows by one per call."""
+    flags and an epoch counter (zero-filled once), W stage rows of up to
+    max_len floats, and the W refusal words."""
 
     def __init__(self, W: int, max_len: int, device="cuda"):
         torch = _torch or _t()
@@ -380,18 +381,23 @@ class OneShotLink:
         self.link = torch.zeros(DETFOLD_ONESHOT_LINK_BYTES // 8, dtype=torch.int64, device=device)
         self.stage = torch.empty(max(1, W * max_len), dtype=torch.float32, device=device)
         self.words = torch.zeros(W, dtype=torch.int32, device=device)
-        self.epoch = 0
 
     def all_reduce(self, arenas, mean_scale: float = 1.0, wait_ns: int = 1_000_000_000,
-                   drop_rank: int = -1, drop_at_exit: bool = False, stream=None) -> None:
+                   drop_rank: int = -1, drop_at_exit: bool = False, stream=None,
+                   epoch: int = 0) -> None:
+        """One call. epoch 0 (the default): the link's device counter supplies
+        the epoch, so the call can be captured in a CUDA graph and replayed;
+        else the caller's epoch, larger than every epoch used on this link."""
         n = arenas[0].numel()
         if n > self.max_len or len(arenas) != self.W:
             raise ValueError("arenas do not fit this link")
-        self.epoch += 1
-        self.words.zero_()
-        detfold_one_shot_allreduce(list(arenas), self.W, n, mean_scale, self.link, self.epoch,
+        detfold_one_shot_allreduce(list(arenas), self.W, n, mean_scale, self.link, epoch,
                                    self.stage, self.words, wait_ns, drop_rank,
                                    1 if drop_at_exit else 0, stream)
+
+    def counter(self) -> int:
+        """The largest epoch used on this link so far (reads the device)."""
+        return int(self.link[2 * DETFOLD_ONESHOT_MAX_CTAS].item())
 
     def barrier_errors(self) -> list[int]:
         """The refusal words of the last call: 0, 40043 (entry) or 40044 (exit)."""

@@ -404,7 +404,7 @@ int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float m
     if (!arenas || !link || !stage || !words) return DETFOLD_ERR_NULL;
     if (W < 1 || W > DETFOLD_ONESHOT_MAX_W) return DETFOLD_ERR_WORLD;
     if (len < 0 || len > DETFOLD_ONESHOT_MAX_LEN) return DETFOLD_ERR_LEN;
-    if (epoch < 1 || wait_ns < 1 || wait_ns > 2000000000LL || drop_rank < -1 || drop_rank >= W)
+    if (wait_ns < 1 || wait_ns > 2000000000LL || drop_rank < -1 || drop_rank >= W)
         return DETFOLD_ERR_ARG;
     if (((uintptr_t)link & 7u) || !aligned4(stage) || ((uintptr_t)words & 3u))
         return DETFOLD_ERR_ALIGN;

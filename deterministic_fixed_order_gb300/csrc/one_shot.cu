@@ -20,6 +20,15 @@
 // expired wait writes the rank's refusal word and returns before step 4, so
 // the arena keeps its old contents. Epoch flags only grow, so a call that
 // refused leaves nothing to reset: the next call's larger epoch starts clean.
+//
+// The epoch comes from the host (>= 1) or, when the host passes 0, from a
+// counter in the link: every CTA reads it before publishing anything and uses
+// counter + 1. Every CTA that ran raises the counter to its epoch (atomicMax)
+// on each way out, so the next call starts above every flag ever published,
+// also after refused calls. In a call that completes, all CTAs read the
+// counter before any of them passes the exit barrier and raises it, so they
+// agree on the epoch. A captured graph therefore replays correctly: each
+// replay takes the next epoch from device memory.
 // For failure-detection tests the host may drop one rank at the entry or the
 // exit barrier (it never publishes there), which makes the others' waits run
 // out by design.
@@ -41,8 +50,9 @@ struct OneShotParams {
     float *stage;                      // W rows of len floats
     unsigned long long *entry_flags;   // DETFOLD_ONESHOT_MAX_CTAS each
     unsigned long long *exit_flags;
+    unsigned long long *counter;       // the link's epoch counter
     int *words;                        // W refusal words
-    unsigned long long epoch;
+    unsigned long long epoch;          // 0: counter + 1
     int64_t len;
     long long wait_ns;
     float scale;
@@ -103,18 +113,31 @@ __device__ bool cta_barrier(unsigned long long *flags, int nctas, unsigned long 
     return s_ok != 0;
 }
 
+__device__ __forceinline__ void raise_counter(const OneShotParams &p, unsigned long long epoch)
+{
+    if (threadIdx.x == 0) atomicMax(p.counter, epoch);
+}
+
 __global__ void __launch_bounds__(kOneShotThreads) one_shot_kernel(const __grid_constant__ OneShotParams p)
 {
     const int r = blockIdx.x / p.ctas_per_rank;
     const int g = blockIdx.x % p.ctas_per_rank;
     const int nctas = gridDim.x;
     const bool dropped = (r == p.drop_rank);
-    if (g == 0 && threadIdx.x == 0 && !dropped) p.words[r] = DETFOLD_OK;
+    __shared__ unsigned long long s_epoch;
+    if (threadIdx.x == 0) s_epoch = p.epoch ? p.epoch : ld_acquire(p.counter) + 1;
+    __syncthreads();
+    const unsigned long long epoch = s_epoch;
+    if (g == 0 && threadIdx.x == 0) p.words[r] = DETFOLD_OK;  // a dropped rank refuses nothing
 
     // 1. entry barrier
-    if (dropped && !p.drop_at_exit) return;  // this rank never joins
-    if (!cta_barrier(p.entry_flags, nctas, p.epoch, p.wait_ns, true)) {
+    if (dropped && !p.drop_at_exit) {  // this rank never joins
+        raise_counter(p, epoch);
+        return;
+    }
+    if (!cta_barrier(p.entry_flags, nctas, epoch, p.wait_ns, true)) {
         if (g == 0 && threadIdx.x == 0) p.words[r] = DETFOLD_ONESHOT_REFUSE_ENTRY;
+        raise_counter(p, epoch);
         return;  // x untouched
     }
 
@@ -129,15 +152,20 @@ __global__ void __launch_bounds__(kOneShotThreads) one_shot_kernel(const __grid_
     }
 
     // 3. exit barrier: every rank has finished reading the arenas
-    if (dropped) return;  // dropped at the exit barrier: never publishes there
-    if (!cta_barrier(p.exit_flags, nctas, p.epoch, p.wait_ns, true)) {
+    if (dropped) {  // dropped at the exit barrier: never publishes there
+        raise_counter(p, epoch);
+        return;
+    }
+    if (!cta_barrier(p.exit_flags, nctas, epoch, p.wait_ns, true)) {
         if (g == 0 && threadIdx.x == 0) p.words[r] = DETFOLD_ONESHOT_REFUSE_EXIT;
+        raise_counter(p, epoch);
         return;  // x untouched
     }
 
     // 4. the stage row becomes the arena
     for (int64_t i = (int64_t)g * blockDim.x + threadIdx.x; i < p.len; i += stride)
         st1(p.arena[r] + i, ld1<false>(stage + i));
+    raise_counter(p, epoch);
 }
 
 }  // namespace
@@ -172,6 +200,7 @@ cudaError_t launch_one_shot(float *const *arenas, int W, int64_t len, float scal
     p.stage = stage;
     p.entry_flags = (unsigned long long *)link;
     p.exit_flags = (unsigned long long *)link + DETFOLD_ONESHOT_MAX_CTAS;
+    p.counter = (unsigned long long *)link + 2 * DETFOLD_ONESHOT_MAX_CTAS;
     p.words = words;
     p.epoch = epoch;
     p.len = len;

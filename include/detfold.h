@@ -186,10 +186,14 @@ int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, f
  *             f32, pairwise disjoint.
  *   len       <= DETFOLD_ONESHOT_MAX_LEN (a small-payload primitive).
  *   link      device, DETFOLD_ONESHOT_LINK_BYTES, 8-byte aligned, zero-filled
- *             once before the first call on it, then reused unchanged.
- *   epoch     >= 1 and larger than every epoch used before on this link (the
- *             barrier flags only grow, so nothing needs resetting after a
- *             refused call).
+ *             once before the first call on it, then reused unchanged: the
+ *             entry and exit barrier flags and an epoch counter.
+ *   epoch     0: the link's counter supplies the epoch (the largest epoch
+ *             used on this link, plus one), so a call captured in a CUDA
+ *             graph replays correctly. >= 1: this epoch, which must be larger
+ *             than every epoch used before on this link. The barrier flags
+ *             and the counter only grow, so nothing needs resetting after a
+ *             refused call.
  *   stage     device, W * len f32 scratch, disjoint from the arenas.
  *   words     device, W ints: rank r's refusal word -- DETFOLD_OK, or
  *             DETFOLD_ONESHOT_REFUSE_ENTRY / _EXIT when its bounded wait at
@@ -206,7 +210,7 @@ int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, f
 #define DETFOLD_ONESHOT_MAX_W 64
 #define DETFOLD_ONESHOT_MAX_LEN ((int64_t)1 << 22)
 #define DETFOLD_ONESHOT_MAX_CTAS 1024
-#define DETFOLD_ONESHOT_LINK_BYTES (2 * DETFOLD_ONESHOT_MAX_CTAS * 8)
+#define DETFOLD_ONESHOT_LINK_BYTES (2 * DETFOLD_ONESHOT_MAX_CTAS * 8 + 64)
 #define DETFOLD_ONESHOT_REFUSE_ENTRY 40043
 #define DETFOLD_ONESHOT_REFUSE_EXIT 40044
 int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
@@ -232,7 +236,8 @@ int detfold_broadcast(float *const *dsts, int ndst, const float *src, int64_t le
  *          pairwise disjoint and disjoint from every part.
  *   parts  host array of W device pointers, each to span f32, read (parts
  *          may overlap each other).
- * One movement launch per part.
+ * With W <= 8 and every pair at one 16-byte phase, one movement launch for
+ * all pairs (each part read once); otherwise one launch per part.
  */
 int detfold_all_gather(float *const *outs, int W, const float *const *parts, int64_t span,
                        void *stream);
@@ -248,7 +253,7 @@ int detfold_all_gather(float *const *outs, int W, const float *const *parts, int
 int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens);
 
 /*
- * Allocation-free staged loopback all-reduce. The paper has no counterpart:
+ * Allocation-free staged loopback all-reduce. The sources have no counterpart:
  * this entry point exists for callers that cannot call cudaMalloc -- code
  * that runs while a stream is being captured into a CUDA graph (allocation
  * is not permitted there), and runtimes whose device memory is owned and

@@ -39,6 +39,40 @@ def test_header_declares_the_api():
         assert want in names
 
 
+def test_binding_constants_match_the_header(df):
+    text = HEADER.read_text() if hasattr(HEADER, "read_text") else open(HEADER).read()
+    defs = dict(re.findall(r"^#define (DETFOLD_\w+) (.+)$", text, re.M))
+
+    import ast
+    import operator
+    ops = {ast.Add: operator.add, ast.Sub: operator.sub, ast.Mult: operator.mul,
+           ast.LShift: operator.lshift, ast.USub: operator.neg}
+
+    def arith(node):  # integer constants, + - * << and unary minus only
+        if isinstance(node, ast.Constant) and isinstance(node.value, int):
+            return node.value
+        if isinstance(node, ast.BinOp) and type(node.op) in ops:
+            return ops[type(node.op)](arith(node.left), arith(node.right))
+        if isinstance(node, ast.UnaryOp) and type(node.op) in ops:
+            return ops[type(node.op)](arith(node.operand))
+        raise ValueError(f"unexpected header expression: {ast.dump(node)}")
+
+    def value(name):
+        expr = re.sub(r"/\*.*", "", defs[name]).strip()
+        expr = expr.replace("(int64_t)", "")
+        expr = re.sub(r"\b(DETFOLD_\w+)\b", lambda m: f"({value(m.group(1))})", expr)
+        return arith(ast.parse(expr, mode="eval").body)
+
+    for name in ("DETFOLD_MAX_W", "DETFOLD_MAX_LEN", "DETFOLD_STAGED_REVERSE_DELIVERY",
+                 "DETFOLD_STAGED_SEPARATE_SCALE", "DETFOLD_STAGED_CE_COPIES",
+                 "DETFOLD_NOALLOC_SCRATCH_BYTES", "DETFOLD_ONESHOT_MAX_W", "DETFOLD_ONESHOT_MAX_LEN",
+                 "DETFOLD_ONESHOT_MAX_CTAS", "DETFOLD_ONESHOT_LINK_BYTES",
+                 "DETFOLD_ONESHOT_REFUSE_ENTRY", "DETFOLD_ONESHOT_REFUSE_EXIT"):
+        assert getattr(df, name) == value(name), name
+    for name, v in df.STATUS.items():
+        assert value(name) == v, name
+
+
 def test_library_exports_every_declared_symbol(df):
     out = subprocess.run(["nm", "-D", "--defined-only", df.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
@@ -229,7 +263,9 @@ def test_validation_one_shot(df):
     assert call(W=0) == S["DETFOLD_ERR_WORLD"]
     assert call(W=65) == S["DETFOLD_ERR_WORLD"]
     assert call(n=(1 << 22) + 1) == S["DETFOLD_ERR_LEN"]
-    assert call(epoch=0) == S["DETFOLD_ERR_ARG"]
+    assert call(epoch=0, n=0) == S["DETFOLD_OK"]  # 0: the link's counter supplies the epoch
+    # the counter sits past the barrier flags and belongs to the link
+    assert call(link=A - df.DETFOLD_ONESHOT_LINK_BYTES + 32) == S["DETFOLD_ERR_OVERLAP"]
     assert call(wait=0) == S["DETFOLD_ERR_ARG"]
     assert call(wait=3_000_000_000) == S["DETFOLD_ERR_ARG"]
     assert call(drop=2) == S["DETFOLD_ERR_ARG"]

@@ -75,3 +75,80 @@ def test_dropped_rank_refuses_and_leaves_arenas_untouched(at_exit):
     oracle.allreduce(want)
     for r in range(W):
         assert_bitwise(arenas[r].host(), want[r], f"rank {r} after recovery")
+
+
+def test_graph_replays_take_fresh_epochs_from_the_link():
+    # With the link's counter supplying the epoch, one captured call replays
+    # as a fresh call each time: the three rounds double the sum, as eagerly.
+    n = 4096
+    a, b = gen.vecf(n, 11 + n), gen.vecf(n, 77 + n)
+    want = oracle.fold(np.stack([a, b]))
+    link = df.OneShotLink(2, n)
+    xa, xb = Guarded(n, 0, a), Guarded(n, 0, b)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        link.all_reduce([xa.t, xb.t])
+    assert link.counter() == 0  # nothing ran during the capture
+    for rnd in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        assert link.barrier_errors() == [0, 0], f"replay {rnd}"
+        assert link.counter() == rnd + 1
+        w = (want.astype(np.float64) * (1 << rnd)).astype(np.float32)
+        assert_bitwise(xa.host(), w, f"rank 0 replay {rnd}")
+        assert_bitwise(xb.host(), w, f"rank 1 replay {rnd}")
+    # a graph of several calls: each node takes the next epoch
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        for _ in range(4):
+            link.all_reduce([xa.t, xb.t])
+    g2.replay()
+    torch.cuda.synchronize()
+    assert link.counter() == 3 + 4
+    w = (want.astype(np.float64) * (1 << 6)).astype(np.float32)
+    assert_bitwise(xa.host(), w, "after a 4-call graph")
+    assert xa.intact() and xb.intact()
+
+
+def test_host_and_device_epochs_mix_on_one_link():
+    W, n = 3, 1000
+    rows = gen.normal_rows(W, n)
+    arenas = [Guarded(n, 0, rows[r]) for r in range(W)]
+    host = [rows[r].copy() for r in range(W)]
+    link = df.OneShotLink(W, n)
+    link.all_reduce([x.t for x in arenas])           # device epoch 1
+    link.all_reduce([x.t for x in arenas], epoch=5)  # host epoch above the counter
+    torch.cuda.synchronize()
+    assert link.counter() == 5  # raised to the host's epoch
+    link.all_reduce([x.t for x in arenas])           # device epoch 6
+    torch.cuda.synchronize()
+    assert link.counter() == 6
+    assert link.barrier_errors() == [0] * W
+    for _ in range(3):
+        oracle.allreduce(host)
+    for r in range(W):
+        assert_bitwise(arenas[r].host(), host[r], f"rank {r}")
+
+
+def test_refused_call_advances_the_counter():
+    # every CTA that published raises the counter, so the next call's epoch
+    # is above every flag the refused call left behind
+    W, n = 4, 4096
+    rows = gen.normal_rows(W, n)
+    arenas = [Guarded(n, 0, rows[r]) for r in range(W)]
+    link = df.OneShotLink(W, n)
+    for at_exit in (False, True):
+        before = link.counter()
+        link.all_reduce([x.t for x in arenas], drop_rank=1, drop_at_exit=at_exit, wait_ns=20_000_000)
+        torch.cuda.synchronize()
+        assert link.counter() == before + 1
+        for r in range(W):
+            assert_bitwise(arenas[r].host(), rows[r], f"rank {r} changed after a refusal")
+    link.all_reduce([x.t for x in arenas])
+    torch.cuda.synchronize()
+    assert link.barrier_errors() == [0] * W
+    want = [rows[r].copy() for r in range(W)]
+    oracle.allreduce(want)
+    for r in range(W):
+        assert_bitwise(arenas[r].host(), want[r], f"rank {r} after the refusals")

@@ -467,6 +467,19 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
     return out
 
 
+def arm_config(world: int) -> dict:
+    """The workload both arms report: one pass of every hot-path row."""
+    return {
+        "workload": "one pass of every hot-path row: C3 W=8x2^26 stacked + ptrs fold, "
+                    "C4 W=4x1e8 fused and staged loopback all-reduce x0.25, "
+                    "C5 W=3,6 x (2^20+7) at base+4B sum/mean/all-reduce, "
+                    "C2 W=2 n=4096 and 65536 small-path folds",
+        "step_algorithmic_bytes": sum(row_bytes().values()),
+        "l2": "inputs larger than L2 (~11 GB per step), no flush",
+        "parallelism": f"replicas x{world} (one independent loopback world per GPU)",
+    }
+
+
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context only)
 
 
@@ -835,15 +848,7 @@ def run_gpu(args) -> None:
         "dtype": "f32",
         "data": "synthetic (seeded xorshift64 generators: C1/C2 vecf, C3 gradient-like, "
                 "C4 normal, C5 stress)",
-        "config": {
-            "workload": "one pass of every hot-path row: C3 W=8x2^26 stacked + ptrs fold, "
-                        "C4 W=4x1e8 fused and staged loopback all-reduce x0.25, "
-                        "C5 W=3,6 x (2^20+7) at base+4B sum/mean/all-reduce, "
-                        "C2 W=2 n=4096 and 65536 small-path folds",
-            "step_algorithmic_bytes": step_bytes,
-            "l2": "inputs larger than L2 (~11 GB per step), no flush",
-            "parallelism": f"replicas x{world} (one independent loopback world per GPU)",
-        },
+        "config": arm_config(world),
         "rows": per_row,
         "roofline": roofline,
         "c2_graph": graph,
@@ -920,11 +925,10 @@ def run_reference(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "CPU oracle over bounded samples of the hot-path step "
-                               "(C3, C4 fused+staged, C5 W=3,6, C2)",
-                   "step_algorithmic_bytes": step_bytes},
+        "config": arm_config(world),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample,
+                         "sample_step_algorithmic_bytes": step_bytes, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)

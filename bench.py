@@ -454,6 +454,31 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
         out[key] = round(statistics.median(ts), 3)  # ms per 1000 calls = us per call
         del g
     out["one_shot_barrier_errors_after_graphs"] = link.barrier_errors()
+    # the C5 rows (sum, mean pass, all-reduce) back to back in a graph of 100
+    # rows: their device time without the per-row event records of the step
+    row_fns = {name: fn for name, fn, _ in wl.rows()}
+    rb = row_bytes()
+    for W in C5_WS:
+        key = f"c5_w{W}"
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            for _ in range(100):
+                row_fns[key]()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(7):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(gs):
+                a.record()
+                g.replay()
+                b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / 100)
+        ms = statistics.median(ts)
+        out[f"{key}_graph"] = {"us": round(ms * 1e3, 2), "gbs": round(rb[key] / (ms * 1e-3) / 1e9, 1)}
+        del g
     # mismatched phases at the C3 size: the rows of an [8][2^26 - 3] stack sit
     # at eight different 4-byte phases, so the realigned kernel runs
     nm = C3_N - 3

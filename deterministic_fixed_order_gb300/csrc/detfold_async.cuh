@@ -56,7 +56,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
 }
 
 // Bounded wait for the phase of parity `parity` to complete.
-static __device__ bool mbar_wait(uint64_t *b, uint32_t parity)
+static __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity)
 {
     const long long t0 = now_ns();
     for (uint32_t i = 0; i < (1u << 22); ++i) {

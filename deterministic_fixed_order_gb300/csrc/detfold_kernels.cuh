@@ -145,6 +145,18 @@ constexpr int max_threads()
     return bw_threads<MODE>() > DETFOLD_SMALL_THREADS ? bw_threads<MODE>() : DETFOLD_SMALL_THREADS;
 }
 
+// CTA size of the vector kernel: the mode's size, halved while a thread's
+// live values -- W*VEC*U loaded floats, W*U 64-bit addresses and about 24
+// registers of indices and loop state -- would exceed the registers that size
+// leaves per thread (65536 / threads), so no instantiation spills.
+template <int W, int VEC, int U, int MODE>
+constexpr int vec_threads()
+{
+    int t = bw_threads<MODE>();
+    while (t > 128 && W * VEC * U + 2 * W * U + 24 > 65536 / t) t /= 2;
+    return t;
+}
+
 constexpr int kGenericW = 256;  // table capacity of the runtime-W kernels
 
 template <int NT>
@@ -302,7 +314,7 @@ __device__ __forceinline__ void store_result(const FoldParams<NT> &p, int64_t e,
 // U vectors per thread per iteration, grid-stride; every operand shares the
 // same VEC*4-byte phase. Element index of vector v is head + v*VEC.
 template <int W, int VEC, int U, int MODE>
-__global__ void __launch_bounds__(max_threads<MODE>()) fold_vec_kernel(const __grid_constant__ FoldParams<W> p)
+__global__ void __launch_bounds__(vec_threads<W, VEC, U, MODE>()) fold_vec_kernel(const __grid_constant__ FoldParams<W> p)
 {
     constexpr bool NC = (MODE == kSumNC);
     pdl_enter(p.pdl);

@@ -174,13 +174,17 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         return exact ? launch_kernel<fold_small_kernel<W, 4, MODE, true>>(p, pl.nvec, 1, true, T, C, stream)
                      : launch_kernel<fold_small_kernel<W, 4, MODE, false>>(p, pl.nvec, 1, true, T, C, stream);
     }
+    // a vector kernel whose CTA was shrunk to fit its registers gets as many
+    // more CTAs per SM as the cap allows, so the threads per SM stay the same
     if (pl.vec == 8) {
         constexpr int U = u_for<MODE>(W, 8);
-        return launch_kernel<fold_vec_kernel<W, 8, U, MODE>>(p, pl.nvec, U, small, T, C, stream);
+        constexpr int VT = vec_threads<W, 8, U, MODE>();
+        return launch_kernel<fold_vec_kernel<W, 8, U, MODE>>(p, pl.nvec, U, small, VT, C * (T / VT), stream);
     }
     if (pl.vec == 4) {
         constexpr int U = u_for<MODE>(W, 4);
-        return launch_kernel<fold_vec_kernel<W, 4, U, MODE>>(p, pl.nvec, U, small, T, C, stream);
+        constexpr int VT = vec_threads<W, 4, U, MODE>();
+        return launch_kernel<fold_vec_kernel<W, 4, U, MODE>>(p, pl.nvec, U, small, VT, C * (T / VT), stream);
     }
     if constexpr (MODE != kAllReduce) {
         // no common phase: realign every source onto the output's 32-byte grid

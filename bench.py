@@ -505,6 +505,38 @@ def arm_config(world: int) -> dict:
     }
 
 
+def host_link_gbs(torch, dev, reps: int = 5) -> dict:
+    """Host<->device link rates in this run, best of `reps`: a 1 GiB copy from
+    pinned host memory to the device, the reverse, and both at once on two
+    streams (bytes of both directions / time)."""
+    n = 1 << 28
+    h_in = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    h_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    d_a = torch.empty(n, dtype=torch.float32, device=dev)
+    d_b = torch.empty(n, dtype=torch.float32, device=dev)
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def best(streams_and_fns, nbytes):
+        top = 0.0
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for st, fn in streams_and_fns:
+                with torch.cuda.stream(st):
+                    fn()
+            torch.cuda.synchronize()
+            top = max(top, nbytes / (time.perf_counter() - t0) / 1e9)
+        return top
+
+    nb = n * 4
+    res = {"h2d_gbs": best([(up, lambda: d_a.copy_(h_in, non_blocking=True))], nb),
+           "d2h_gbs": best([(down, lambda: h_out.copy_(d_b, non_blocking=True))], nb),
+           "both_gbs": best([(up, lambda: d_a.copy_(h_in, non_blocking=True)),
+                             (down, lambda: h_out.copy_(d_b, non_blocking=True))], 2 * nb)}
+    del h_in, h_out, d_a, d_b
+    return res
+
+
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context only)
 
 
@@ -838,6 +870,8 @@ def run_gpu(args) -> None:
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e_value = whole_job_gbs(world, step_bytes, e2e_ms)
+    link = host_link_gbs(torch, dev)
+    link_gbs = (h2d + d2h) / (e2e_ms * 1e-3) / 1e9
     # every step starts from the host inputs, so the read-back is one step
     e2e_check = 0
     idx = np.arange(0, C3_N, 16411)
@@ -887,7 +921,10 @@ def run_gpu(args) -> None:
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                 "pipelined": "per-row H2D and D2H streams around one compute stream",
-                "bitwise_sampled_words_differing": int(e2e_check)},
+                "bitwise_sampled_words_differing": int(e2e_check),
+                "link_bytes_gbs": round(link_gbs, 1),
+                "link_this_run": {k: round(v, 1) for k, v in link.items()},
+                "link_utilisation_of_both_ways": round(link_gbs / link["both_gbs"], 3)},
         "gpu_launches": launches,
         "clocks": clock_summary,
         "cpu_baseline": cpu,

@@ -1,10 +1,13 @@
 """Run one fold row at a chosen size for a few launches (for profiler captures).
 
-    python -m deterministic_fixed_order_gb300.profile_case ROW --len N [--W W] [--launches K]
+    python -m deterministic_fixed_order_gb300.profile_case ROW --len N [--W W] [--launches K] [--offset E]
 
 ROW is one of: stacked, ptrs, allreduce, staged, scale, small. Inputs are
-seeded synthetic data. Parity of these calls is established by the test
-suite; this runner only launches them and reports the status.
+seeded synthetic data. --offset E starts every operand E elements past an
+allocation boundary (E = 1 is the odd-world stress layout, base + 4 bytes;
+stacked keeps its rows contiguous after the offset). Parity of these calls is
+established by the test suite; this runner only launches them and reports
+the status.
 """
 from __future__ import annotations
 
@@ -23,7 +26,10 @@ def main() -> int:
     ap.add_argument("--len", type=int, required=True)
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--offset", type=int, default=0)
     a = ap.parse_args()
+    if not 0 <= a.offset < 64:
+        ap.error("--offset must be in [0, 64)")
 
     import torch
 
@@ -31,10 +37,17 @@ def main() -> int:
     import detfold_inputs as gen
 
     dev = torch.device("cuda:0")
-    W, n = a.W, a.len
+    W, n, off = a.W, a.len, a.offset
     rows = gen.gradient_rows(W, n)
-    d = torch.from_numpy(rows).to(dev)
-    out = torch.empty(n, dtype=torch.float32, device=dev)
+    if a.row in ("stacked", "small"):
+        flat = torch.empty(W * n + off, dtype=torch.float32, device=dev)
+        d = flat[off:].view(W, n)
+        d.copy_(torch.from_numpy(rows))
+    else:  # one allocation per operand, each at the offset
+        d = [torch.empty(n + off, dtype=torch.float32, device=dev)[off:] for _ in range(W)]
+        for r in range(W):
+            d[r].copy_(torch.from_numpy(rows[r]))
+    out = torch.empty(n + off, dtype=torch.float32, device=dev)[off:]
     if a.row in ("stacked", "small"):
         fn = lambda: df.detfold_sum_stacked(out, d, W, n)
     elif a.row == "ptrs":

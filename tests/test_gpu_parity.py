@@ -322,12 +322,13 @@ def test_broadcast_and_all_gather_move_bytes_exactly(span, W):
 
 
 @pytest.mark.parametrize("span", [1, 7, 1024, 4099, 16384, 1 << 17, (1 << 17) + 1])
-@pytest.mark.parametrize("W", [2, 3, 8])
+@pytest.mark.parametrize("W", [2, 3, 8, 12])
 @pytest.mark.parametrize("off", [0, 1, 4, 7])
 def test_movement_at_one_phase_with_heads_and_tails(span, W, off):
     # Every pointer at one phase: the vector movement kernels, with a head and
     # a tail at offsets 1 and 7; spans up to 2^17 take the small-move kernel
-    # (one pair-vector per thread), 2^17 + 1 the looping kernel.
+    # (one pair-vector per thread), 2^17 + 1 the looping kernel. W = 12 parts
+    # is past the one-launch all-gather (at most 8 parts): one launch per part.
     src_h = _random_bits(span, 57 + span)
     src = Guarded(span, off, src_h)
     dsts = [Guarded(span, off) for _ in range(W - 1)]
@@ -347,12 +348,15 @@ def test_movement_at_one_phase_with_heads_and_tails(span, W, off):
         assert_bitwise(o.host(), want, f"all-gather span={span} off={off} rank={r}")
 
 
-def test_broadcast_many_destinations_splits_launches():
-    # more destinations than one parameter block holds
-    span, nd = 1000, 256
+@pytest.mark.parametrize("layout", ["mixed", "aligned", "aligned+head"])
+def test_broadcast_many_destinations_splits_launches(layout):
+    # more destinations than one parameter block holds (250 pairs per launch):
+    # mixed phases take the scalar kernel, one phase the small-move kernel
+    span, nd = (1003 if layout == "aligned+head" else 1000), 256
     src_h = _random_bits(span, 7)
-    src = Guarded(span, 0, src_h)
-    dsts = [Guarded(span, r % 8) for r in range(nd)]
+    off = {"mixed": 0, "aligned": 0, "aligned+head": 1}[layout]
+    src = Guarded(span, off, src_h)
+    dsts = [Guarded(span, r % 8 if layout == "mixed" else off) for r in range(nd)]
     df.detfold_broadcast([d.t for d in dsts], nd, src.t, span)
     sync()
     for d in dsts:

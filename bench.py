@@ -272,45 +272,54 @@ class Workload:
         return out
 
 
-def sampled_check(wl, steps_run: int, torch, oracle, rng) -> dict:
-    """Bit-exact check of the bench's own outputs on sampled columns: the
-    oracle replays the same number of steps on those columns (all-reduces
-    are in place, so their state after k steps is k repeated all-reduces)."""
-    res = {}
+def collect_step_samples(wl, steps_run: int, rng) -> list[dict]:
+    """Host copies of the bench's own outputs on sampled columns, with the
+    host inputs those columns came from (no oracle here: `verify_samples`, in
+    the oracle leg, computes what they must be). The all-reduces are in place,
+    so after k steps their state is k repeated all-reduces."""
+    specs = []
     idx3 = np.sort(rng.choice(C3_N, 4096, replace=False))
-    rows3 = wl.h_c3.numpy().reshape(C3_W, C3_N)[:, idx3]
-    want3 = oracle.fold_stacked(np.ascontiguousarray(rows3))
-    got = wl.c3_out.cpu().numpy()[idx3]
-    got2 = wl.c3_out2.cpu().numpy()[idx3]
-    res["c3"] = int(oracle.bit_diffs(got, want3) + oracle.bit_diffs(got2, want3))
+    rows3 = np.ascontiguousarray(wl.h_c3.numpy().reshape(C3_W, C3_N)[:, idx3])
+    specs.append({"group": "c3", "kind": "fold_stacked", "inputs": rows3,
+                  "got": [wl.c3_out.cpu().numpy()[idx3], wl.c3_out2.cpu().numpy()[idx3]]})
     idx4 = np.sort(rng.choice(C4_N, 4096, replace=False))
     h4 = wl.h_c4.numpy().reshape(C4_W, C4_N)
-    ar = [np.ascontiguousarray(h4[r, idx4]) for r in range(C4_W)]
-    for _ in range(steps_run):
-        oracle.allreduce(ar, np.float32(wl.scale4))
-    d = 0
-    for r in range(C4_W):
-        d += oracle.bit_diffs(wl.c4f[r].cpu().numpy()[idx4], ar[r])
-        d += oracle.bit_diffs(wl.c4s[r].cpu().numpy()[idx4], ar[r])
-    res["c4"] = int(d)
-    d = 0
+    specs.append({"group": "c4", "kind": "allreduce", "repeat": steps_run, "scale": wl.scale4,
+                  "inputs": [np.ascontiguousarray(h4[r, idx4]) for r in range(C4_W)],
+                  "got": [[wl.c4f[r].cpu().numpy()[idx4] for r in range(C4_W)],
+                          [wl.c4s[r].cpu().numpy()[idx4] for r in range(C4_W)]]})
     for W in C5_WS:
         h5 = wl.h_c5[W].numpy().reshape(W, C5_N)
         idx5 = np.r_[0:16, np.sort(rng.choice(np.arange(16, C5_N), 2048, replace=False))]
-        want = oracle.scale(oracle.fold(np.ascontiguousarray(h5[:, idx5])), np.float32(wl.scale5[W]))
-        d += oracle.bit_diffs(wl.c5_out[W].cpu().numpy()[idx5], want)
-        ar = [np.ascontiguousarray(h5[r, idx5]) for r in range(W)]
-        for _ in range(steps_run):
-            oracle.allreduce(ar, np.float32(wl.scale5[W]))
-        for r in range(W):
-            d += oracle.bit_diffs(wl.c5_ar[W][r].cpu().numpy()[idx5], ar[r])
-    res["c5"] = int(d)
-    d = 0
+        cols = np.ascontiguousarray(h5[:, idx5])
+        specs.append({"group": "c5", "kind": "fold_scale", "inputs": cols, "scale": wl.scale5[W],
+                      "got": [wl.c5_out[W].cpu().numpy()[idx5]]})
+        specs.append({"group": "c5", "kind": "allreduce", "repeat": steps_run, "scale": wl.scale5[W],
+                      "inputs": [np.ascontiguousarray(cols[r]) for r in range(W)],
+                      "got": [[wl.c5_ar[W][r].cpu().numpy()[idx5] for r in range(W)]]})
     for n in C2_NS:
-        want = oracle.fold_stacked(wl.h_c2[n].numpy().reshape(2, n))
-        d += oracle.bit_diffs(wl.c2_out[n].cpu().numpy(), want)
-    res["c2"] = int(d)
-    res["words_differing"] = int(sum(res.values()))
+        specs.append({"group": "c2", "kind": "fold_stacked", "inputs": wl.h_c2[n].numpy().reshape(2, n),
+                      "got": [wl.c2_out[n].cpu().numpy()]})
+    return specs
+
+
+def verify_samples(oracle, specs: list[dict]) -> dict:
+    """Words that differ from the oracle, by group, for collected samples."""
+    res = {}
+    for sp in specs:
+        if sp["kind"] == "fold_stacked":
+            want = [oracle.fold_stacked(sp["inputs"])]
+            gots = [[g] for g in sp["got"]]
+        elif sp["kind"] == "fold_scale":
+            want = [oracle.scale(oracle.fold(sp["inputs"]), np.float32(sp["scale"]))]
+            gots = [[g] for g in sp["got"]]
+        else:  # allreduce, repeated
+            want = [a.copy() for a in sp["inputs"]]
+            for _ in range(sp["repeat"]):
+                oracle.allreduce(want, np.float32(sp["scale"]))
+            gots = sp["got"]
+        d = sum(oracle.bit_diffs(g, w) for got in gots for g, w in zip(got, want))
+        res[sp["group"]] = res.get(sp["group"], 0) + int(d)
     return res
 
 
@@ -370,6 +379,12 @@ def graph_us_per_call(torch, df, wl, rounds: int = 5, reps: int = 5) -> dict:
         res.setdefault(group, {})[key] = round(statistics.median(ts), 3)
     res["floors"]["spread_us"] = round(max(max(v) - min(v) for v in times.values()), 3)
     del graphs
+    # the bits after all the replays must equal one fold: every word goes to
+    # the oracle leg
+    torch.cuda.synchronize()
+    res["_specs"] = [{"group": f"c2_{n}_after_graph_replays", "kind": "fold_stacked",
+                      "inputs": wl.h_c2[n].numpy().reshape(2, n), "got": [wl.c2_out[n].cpu().numpy()]}
+                     for n in C2_NS]
     return res
 
 
@@ -593,6 +608,16 @@ def cpu_model() -> str:
     return "unknown"
 
 
+def oracle_leg(gen, world: int, samples: list[dict]) -> tuple[dict | None, dict]:
+    """The bench's oracle leg, the one place the GPU arm uses the CPU oracle:
+    it replays the oracle on the samples the GPU arm collected (words that
+    differ, by group), and at N=1 times the oracle on host cores
+    (cpu_baseline). The GPU arm itself never calls the oracle."""
+    import oracle
+    checks = verify_samples(oracle, samples)
+    return (cpu_baseline(oracle, gen) if world == 1 else None), checks
+
+
 def cpu_baseline(oracle, gen, budget_s: float = 12.0, split_budget_s: float = 4.0) -> dict:
     """The oracle as it stands on a bounded sample of every row of the step:
     the first S elements of each rank's arena (S = 2^21 for the large rows,
@@ -772,11 +797,11 @@ def run_gpu(args) -> None:
                 "frac_of_stream_kernel_this_run": round(achieved / peaks_run["stream_kernel_gbs"], 4),
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)}
 
-    import oracle
     rng = np.random.default_rng(1234)
-    check = sampled_check(wl, steps_done, torch, oracle, rng)
+    step_samples = collect_step_samples(wl, steps_done, rng)
 
     graph = graph_us_per_call(torch, df, wl)
+    graph_samples = graph.pop("_specs")
     extra_rows = next_rows(torch, df, wl)
 
     # End to end through the public API with host buffers: every step copies
@@ -873,23 +898,29 @@ def run_gpu(args) -> None:
     link = host_link_gbs(torch, dev)
     link_gbs = (h2d + d2h) / (e2e_ms * 1e-3) / 1e9
     # every step starts from the host inputs, so the read-back is one step
-    e2e_check = 0
     idx = np.arange(0, C3_N, 16411)
-    want3 = oracle.fold_stacked(np.ascontiguousarray(wl.h_c3.numpy().reshape(C3_W, C3_N)[:, idx]))
-    e2e_check += oracle.bit_diffs(h_out["c3"].numpy()[idx], want3)
     idx4 = np.arange(0, C4_N, 24593)
-    ar = [np.ascontiguousarray(wl.h_c4.numpy().reshape(C4_W, C4_N)[r, idx4]) for r in range(C4_W)]
-    oracle.allreduce(ar, np.float32(wl.scale4))
-    for r in range(C4_W):
-        e2e_check += oracle.bit_diffs(h_out["c4f"].numpy()[r * C4_N + idx4], ar[r])
-        e2e_check += oracle.bit_diffs(h_out["c4s"].numpy()[r * C4_N + idx4], ar[r])
+    h4 = wl.h_c4.numpy().reshape(C4_W, C4_N)
+    e2e_samples = [
+        {"group": "e2e", "kind": "fold_stacked",
+         "inputs": np.ascontiguousarray(wl.h_c3.numpy().reshape(C3_W, C3_N)[:, idx]),
+         "got": [h_out["c3"].numpy()[idx]]},
+        {"group": "e2e", "kind": "allreduce", "repeat": 1, "scale": wl.scale4,
+         "inputs": [np.ascontiguousarray(h4[r, idx4]) for r in range(C4_W)],
+         "got": [[h_out["c4f"].numpy()[r * C4_N + idx4] for r in range(C4_W)],
+                 [h_out["c4s"].numpy()[r * C4_N + idx4] for r in range(C4_W)]]},
+    ]
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
-    cpu = cpu_baseline(oracle, gen) if world == 1 else None
+    cpu, check = oracle_leg(gen, world, step_samples + graph_samples + e2e_samples)
+    for n in C2_NS:
+        graph[str(n)]["words_differing_after_replays"] = check.pop(f"c2_{n}_after_graph_replays")
+    e2e_check = check.pop("e2e")
+    check["words_differing"] = int(sum(check.values()))
 
     line = {
         "metric": METRIC,

@@ -48,3 +48,45 @@ def test_reference_arm_prints_one_json_line():
                 "higher_is_better", "cpu_baseline", "e2e", "impl"):
         assert key in d, key
     assert d["impl"] == "reference" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_verify_samples_counts_differing_words():
+    # the oracle leg's check of collected samples: exact outputs give 0, and a
+    # planted wrong word is counted once per sample it sits in
+    import numpy as np
+
+    import detfold_inputs as gen
+    import oracle
+    rows = gen.stress_rows(3, 257)
+    fold = oracle.fold(rows)
+    scale = oracle.mean_scale(3)
+    arenas = [r.copy() for r in rows]
+    for _ in range(2):
+        oracle.allreduce(arenas, scale)
+    specs = [
+        {"group": "a", "kind": "fold_stacked", "inputs": rows, "got": [fold.copy(), fold.copy()]},
+        {"group": "b", "kind": "fold_scale", "inputs": rows, "scale": scale,
+         "got": [oracle.scale(fold, scale)]},
+        {"group": "c", "kind": "allreduce", "repeat": 2, "scale": scale,
+         "inputs": [r.copy() for r in rows], "got": [[a.copy() for a in arenas]]},
+    ]
+    assert bench.verify_samples(oracle, specs) == {"a": 0, "b": 0, "c": 0}
+    specs[0]["got"][1][5] = np.nextafter(specs[0]["got"][1][5], np.float32(np.inf))
+    specs[2]["got"][0][2][100] = -specs[2]["got"][0][2][100] if specs[2]["got"][0][2][100] != 0 else 1.0
+    assert bench.verify_samples(oracle, specs) == {"a": 1, "b": 0, "c": 1}
+    # the inputs are left as they were (the repeated all-reduce works on copies)
+    assert all(np.array_equal(a.view(np.uint32), r.view(np.uint32)) for a, r in zip(specs[2]["inputs"], rows))
+
+
+def test_gpu_arm_calls_the_oracle_only_through_its_oracle_leg():
+    # bench.py may use the CPU oracle only to time it and to check samples:
+    # run_gpu itself holds no oracle call
+    import ast
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    fn = next(n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "run_gpu")
+    names = {n.id for n in ast.walk(fn) if isinstance(n, ast.Name)}
+    attrs = {n.value.id for n in ast.walk(fn)
+             if isinstance(n, ast.Attribute) and isinstance(n.value, ast.Name)}
+    imports = {a.name for n in ast.walk(fn) if isinstance(n, (ast.Import, ast.ImportFrom))
+               for a in n.names}
+    assert "oracle" not in names | attrs | imports

@@ -379,8 +379,8 @@ def test_c2_small_path_and_graph_replay(n):
     stream.synchronize()
     out.t.zero_()
     sync()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(200):
+    with torch.cuda.graph(g, stream=stream):  # C2: 10,000 back-to-back folds in one graph
+        for _ in range(10_000):
             df.detfold_sum_stacked(out.t, st.t, 2, n)
     for _ in range(3):
         g.replay()

@@ -67,6 +67,12 @@
 #ifndef DETFOLD_SMALL_EXACT
 #define DETFOLD_SMALL_EXACT 1  // small-path kernel without the bounds test when the grid is exact
 #endif
+#ifndef DETFOLD_TINY_VECS
+#define DETFOLD_TINY_VECS 0  // small-path calls of at most this many vectors use DETFOLD_TINY_THREADS
+#endif
+#ifndef DETFOLD_TINY_THREADS
+#define DETFOLD_TINY_THREADS 32
+#endif
 #ifndef DETFOLD_SMALL_THREADS
 #define DETFOLD_SMALL_THREADS 128
 #endif

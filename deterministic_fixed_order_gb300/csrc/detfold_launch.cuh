@@ -132,6 +132,27 @@ inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool smal
     return cudaLaunchKernelEx(&cfg, Kernel, p);
 }
 
+// A small-path launch: ceil(work / threads) CTAs of `threads`, always with
+// programmatic dependent launch when the parameters ask for it.
+template <auto Kernel, typename Params>
+inline cudaError_t launch_small(const Params &p, int64_t work, int threads, cudaStream_t stream)
+{
+    int64_t blocks = (work + threads - 1) / threads;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, Kernel, p);
+}
+
 template <int NT>
 inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool small)
 {
@@ -167,12 +188,14 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
     constexpr int T = bw_threads<MODE>();
     constexpr int C = ctas_per_sm_cap<MODE>();
     if (small && pl.vec != 0) {
-        const bool exact = DETFOLD_SMALL_EXACT && pl.nvec > 0 && pl.nvec % DETFOLD_SMALL_THREADS == 0;
+        // the fewest vectors take smaller CTAs, spread over more SMs
+        const int threads = pl.nvec <= DETFOLD_TINY_VECS ? DETFOLD_TINY_THREADS : DETFOLD_SMALL_THREADS;
+        const bool exact = DETFOLD_SMALL_EXACT && pl.nvec > 0 && pl.nvec % threads == 0;
         if (pl.vec == 8)
-            return exact ? launch_kernel<fold_small_kernel<W, 8, MODE, true>>(p, pl.nvec, 1, true, T, C, stream)
-                         : launch_kernel<fold_small_kernel<W, 8, MODE, false>>(p, pl.nvec, 1, true, T, C, stream);
-        return exact ? launch_kernel<fold_small_kernel<W, 4, MODE, true>>(p, pl.nvec, 1, true, T, C, stream)
-                     : launch_kernel<fold_small_kernel<W, 4, MODE, false>>(p, pl.nvec, 1, true, T, C, stream);
+            return exact ? launch_small<fold_small_kernel<W, 8, MODE, true>>(p, pl.nvec, threads, stream)
+                         : launch_small<fold_small_kernel<W, 8, MODE, false>>(p, pl.nvec, threads, stream);
+        return exact ? launch_small<fold_small_kernel<W, 4, MODE, true>>(p, pl.nvec, threads, stream)
+                     : launch_small<fold_small_kernel<W, 4, MODE, false>>(p, pl.nvec, threads, stream);
     }
     // a vector kernel whose CTA was shrunk to fit its registers gets as many
     // more CTAs per SM as the cap allows, so the threads per SM stay the same

@@ -16,7 +16,8 @@
  *
  * Conventions shared by every entry point:
  *   - Return value: DETFOLD_OK (0) or a negative DETFOLD_ERR_* code. No
- *     entry point aborts, prints, synchronizes or allocates device memory.
+ *     entry point aborts, prints or allocates device memory, and none
+ *     synchronizes except the diagnostic detfold_pipeline_timeouts.
  *     On any error nothing has been enqueued, except DETFOLD_ERR_CUDA from
  *     a multi-launch call, where earlier launches may already be enqueued.
  *   - Pointers named "device" are caller-owned device memory of the current

@@ -67,8 +67,28 @@ static __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity)
     return false;
 }
 
+#ifndef DETFOLD_BULK_L2_HINT
+#define DETFOLD_BULK_L2_HINT 0  // 1: loads evict-first in L2, 2: stores, 3: both
+#endif
+
+// An L2 cache policy that marks lines for early eviction (streamed once).
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
+#if DETFOLD_BULK_L2_HINT & 1
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(evict_first_policy())
+        : "memory");
+    return;
+#endif
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(dst)),
@@ -78,6 +98,12 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 
 __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
 {
+#if DETFOLD_BULK_L2_HINT & 2
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_addr(src)), "r"(bytes), "l"(evict_first_policy())
+                 : "memory");
+    return;
+#endif
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                  "r"(smem_addr(src)), "r"(bytes)
                  : "memory");

@@ -53,7 +53,9 @@ def test_device_c_program_matches_oracle(tmp_path):
     _build("device_fold.c", exe, cflags=["-I", os.path.join(CUDA, "include")],
            ldflags=["-L", os.path.join(CUDA, "lib64"), "-lcudart",
                     f"-Wl,-rpath,{os.path.join(CUDA, 'lib64')}"])
-    for W, n in ((3, (1 << 20) + 7), (4, 100_003), (8, 4099)):
+    # realigned and bulk-async paths, the small path, the 16 KiB decode join
+    # (exact small grid) and an aligned stack on the bulk path
+    for W, n in ((3, (1 << 20) + 7), (4, 100_003), (8, 4099), (2, 4096), (4, (1 << 20) + 4096)):
         rows = gen.stress_rows(W, n)
         inp, outp = tmp_path / "in.bin", tmp_path / "out.bin"
         rows.tofile(inp)

@@ -26,7 +26,7 @@ BOUNDARIES = [1, 3, 4, 7, 8, 9, 1023, 1024, 1025, 2047, 2048, 2049, 4096 + 5,
               SMALL - 1, SMALL, SMALL + 1, SMALL + 7,
               BULK - 1, BULK, BULK + 1, BULK + 7, BULK + 1023, BULK + 2047, BULK + 2048, BULK + 4095]
 ENTRIES = ["stacked", "ptrs", "in_place", "allreduce", "staged", "table_sum", "table_allreduce",
-           "broadcast", "all_gather"]
+           "broadcast", "all_gather", "one_shot", "staged_noalloc"]
 
 
 def _cases(count=480, seed=20261202):
@@ -38,6 +38,8 @@ def _cases(count=480, seed=20261202):
         n = int(rng.choice(BOUNDARIES)) if rng.random() < 0.7 else int(np.exp(rng.uniform(0, np.log(3 * BULK))))
         if entry == "all_gather":
             n = min(n, BULK + 4095)
+        if entry == "staged_noalloc":  # within the library's 16 MiB of scratch
+            n = min(n, 600_000)
         phase = rng.random()
         if phase < 0.4:      # every operand at one phase
             off = int(rng.integers(0, 8))
@@ -86,7 +88,7 @@ def test_random_case_matches_oracle(case):
         torch.cuda.synchronize()
         assert out.intact() and all(s.intact() for s in srcs), what
         assert_bitwise(out.host(), oracle.fold(rows), what)
-    elif entry in ("allreduce", "staged", "table_allreduce"):
+    elif entry in ("allreduce", "staged", "table_allreduce", "one_shot", "staged_noalloc"):
         scale = float(oracle.mean_scale(W)) if seed % 2 else 1.0
         arenas = [Guarded(n, offs[r], rows[r]) for r in range(W)]
         ts = [a.t for a in arenas]
@@ -94,6 +96,13 @@ def test_random_case_matches_oracle(case):
             df.detfold_loopback_allreduce(ts, W, n, scale)
         elif entry == "table_allreduce":
             df.detfold_loopback_allreduce_dev(df.device_table(ts), W, n, scale)
+        elif entry == "one_shot":
+            link = df.OneShotLink(W, n)
+            link.all_reduce(ts, scale)
+            torch.cuda.synchronize()
+            assert link.barrier_errors() == [0] * W, what
+        elif entry == "staged_noalloc":
+            df.detfold_loopback_allreduce_staged_noalloc(ts, W, n, scale, seed % 8)
         else:
             nb = df.detfold_staged_workspace_bytes(n, W)
             ws = torch.empty(max(1, nb // 4), dtype=torch.float32, device="cuda")

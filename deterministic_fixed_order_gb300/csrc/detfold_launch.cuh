@@ -173,6 +173,11 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
 // Bulk-async (TMA) staged bandwidth path (fold_bulk.cu).
 int bulk_tile_floats(int W);
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream);
+// Large fold or all-reduce over a device-resident pointer table, W <= 8: the
+// bulk-async pipeline when the entries share a 16-byte phase (decided on the
+// device), else a scalar fold; same status word as the other table kernels.
+cudaError_t launch_bulk_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
+                              float scale, int do_scale, int mode, cudaStream_t stream);
 cudaError_t read_pipeline_timeouts_bulk(unsigned long long *count);
 cudaError_t read_pipeline_timeouts_move(unsigned long long *count);
 

@@ -127,25 +127,45 @@ __device__ __forceinline__ void bulk_edges(const BulkParams<W> &p, int tc)
     }
 }
 
-template <int W, int MODE>
-__global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const __grid_constant__ BulkParams<W> p)
+// The dynamic shared memory of a bulk CTA: S stages of W input tiles and one
+// result tile, then the full and empty mbarriers of every stage.
+template <int W>
+struct BulkSmem {
+    float *in;        // [S][W][T]
+    float *res;       // [S][T]
+    uint64_t *full;   // [S]
+    uint64_t *empty;  // [S]
+};
+
+template <int W>
+__device__ __forceinline__ BulkSmem<W> bulk_smem_init(unsigned char *smem)
 {
     using Sh = BulkShape<W>;
-    constexpr int T = Sh::T, S = Sh::S, NC = 32 * Sh::NCW;
-    extern __shared__ __align__(128) unsigned char smem[];
-    float *in = (float *)smem;                       // [S][W][T]
-    float *res = in + (size_t)S * W * T;             // [S][T]
-    uint64_t *full = (uint64_t *)(res + (size_t)S * T);
-    uint64_t *empty = full + S;
+    BulkSmem<W> m;
+    m.in = (float *)smem;
+    m.res = m.in + (size_t)Sh::S * W * Sh::T;
+    m.full = (uint64_t *)(m.res + (size_t)Sh::S * Sh::T);
+    m.empty = m.full + Sh::S;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < Sh::S; ++s) {
+            mbar_init(&m.full[s], 1);
+            mbar_init(&m.empty[s], 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    pdl_enter(p.pdl);
-    __syncthreads();
+    return m;
+}
+
+// The pipeline of one CTA, after its mbarriers are initialized and visible:
+// the producer lane streams the CTA's tiles, the consumer warps fold them
+// and store the results, and first fold the call's edges.
+template <int W, int MODE>
+__device__ __forceinline__ void bulk_run(const BulkParams<W> &p, const BulkSmem<W> &m)
+{
+    using Sh = BulkShape<W>;
+    constexpr int T = Sh::T, S = Sh::S, NC = 32 * Sh::NCW;
+    float *in = m.in, *res = m.res;
+    uint64_t *full = m.full, *empty = m.empty;
 
     if (threadIdx.x < 32) {  // producer warp: one lane issues the loads
         if (threadIdx.x == 0) {
@@ -210,9 +230,94 @@ __global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const 
     if (tc == 0) bulk_wait_all();
 }
 
-// Shared-memory opt-in and resident CTAs, once per kernel and device.
 template <int W, int MODE>
-cudaError_t bulk_grid(int *grid)
+__global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const __grid_constant__ BulkParams<W> p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const BulkSmem<W> m = bulk_smem_init<W>(smem);
+    pdl_enter(p.pdl);
+    __syncthreads();
+    bulk_run<W, MODE>(p, m);
+}
+
+// A large fold or all-reduce over a device-resident pointer table.
+struct BulkTableParams {
+    const float *const *table;  // device array of W device pointers
+    float *out;                 // sum mode only
+    int *status;                // optional device status word
+    int64_t len;
+    float scale;
+    int do_scale;
+    int pdl;
+};
+
+// The table is read on the device after the wait (the preceding work may
+// have written it). Every entry is checked as the other table kernels check
+// it (NULL, 4-byte alignment, in rank order, with the status word written
+// and nothing else touched on a bad entry). When every entry (and the
+// output) shares one 16-byte phase, the CTA runs the same bulk pipeline as
+// fold_bulk_kernel; otherwise the grid folds with coalesced scalar accesses.
+template <int W, int MODE>
+__global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_table_kernel(const __grid_constant__ BulkTableParams tp)
+{
+    constexpr int T = BulkShape<W>::T;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ BulkParams<W> sp;
+    __shared__ int s_code, s_bulk;
+    const BulkSmem<W> m = bulk_smem_init<W>(smem);
+    pdl_enter(tp.pdl);
+    if (threadIdx.x == 0) {
+        int code = DETFOLD_OK;
+        for (int r = 0; r < W; ++r) {
+            float *q = const_cast<float *>(tp.table[r]);
+            if (code == DETFOLD_OK && q == nullptr) code = DETFOLD_ERR_NULL;
+            if (code == DETFOLD_OK && ((uintptr_t)q & 3u)) code = DETFOLD_ERR_ALIGN;
+            sp.a[r] = q;
+        }
+        int bulk = 0;
+        if (code == DETFOLD_OK) {
+            const uintptr_t ph = (uintptr_t)sp.a[0] & 15u;
+            bool same = (MODE == kAllReduce) || ((uintptr_t)tp.out & 15u) == ph;
+            for (int r = 1; r < W; ++r) same = same && ((uintptr_t)sp.a[r] & 15u) == ph;
+            int64_t head = (int64_t)(((16u - ph) & 15u) / 4u);
+            if (head > tp.len) head = tp.len;
+            sp.out = tp.out;
+            sp.len = tp.len;
+            sp.head = head;
+            sp.ntiles = (tp.len - head) / T;
+            sp.scale = tp.scale;
+            sp.do_scale = tp.do_scale;
+            sp.pdl = tp.pdl;
+            bulk = same && sp.ntiles >= 1;
+        }
+        s_code = code;
+        s_bulk = bulk;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && tp.status) *tp.status = s_code;
+    if (s_code != DETFOLD_OK) return;
+    if (s_bulk) {
+        bulk_run<W, MODE>(sp, m);
+        return;
+    }
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < tp.len; i += stride) {
+        float acc = ld1<false>(sp.a[0] + i);
+#pragma unroll
+        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<false>(sp.a[r] + i));
+        if (tp.do_scale) acc = __fmul_rn(acc, tp.scale);
+        if constexpr (MODE == kAllReduce) {
+#pragma unroll
+            for (int r = 0; r < W; ++r) st1(sp.a[r] + i, acc);
+        } else {
+            st1(tp.out + i, acc);
+        }
+    }
+}
+
+// Shared-memory opt-in and resident CTAs, once per kernel and device.
+template <auto Kernel, int W>
+cudaError_t bulk_grid_of(int *grid)
 {
     static std::atomic<int> cache[64];
     int dev = 0;
@@ -222,13 +327,13 @@ cudaError_t bulk_grid(int *grid)
     int v = cache[dev].load(std::memory_order_relaxed);
     if (v <= 0) {
         using Sh = BulkShape<W>;
-        e = cudaFuncSetAttribute(fold_bulk_kernel<W, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)Sh::SMEM);
         if (e != cudaSuccess) return e;
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fold_bulk_kernel<W, MODE>, Sh::THREADS,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kernel, Sh::THREADS,
                                                           Sh::SMEM);
         if (e != cudaSuccess) return e;
         if (DETFOLD_BULK_CTAS_PER_SM > 0 && per_sm > DETFOLD_BULK_CTAS_PER_SM) per_sm = DETFOLD_BULK_CTAS_PER_SM;
@@ -253,7 +358,7 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
     p.do_scale = s.do_scale;
     p.pdl = DETFOLD_PDL_ALL ? 1 : 0;
     int cap = 0;
-    cudaError_t e = bulk_grid<W, MODE>(&cap);
+    cudaError_t e = bulk_grid_of<fold_bulk_kernel<W, MODE>, W>(&cap);
     if (e != cudaSuccess) return e;
     int64_t grid = p.ntiles < cap ? p.ntiles : cap;
     if (grid < 1) grid = 1;
@@ -270,6 +375,46 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, fold_bulk_kernel<W, MODE>, p);
+}
+
+template <int W, int MODE>
+cudaError_t launch_bulk_table_fixed(const BulkTableParams &tp, cudaStream_t stream)
+{
+    using Sh = BulkShape<W>;
+    int cap = 0;
+    cudaError_t e = bulk_grid_of<fold_bulk_table_kernel<W, MODE>, W>(&cap);
+    if (e != cudaSuccess) return e;
+    int64_t grid = tp.len / Sh::T;  // about one CTA per tile, at most the resident CTAs
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(Sh::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (tp.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fold_bulk_table_kernel<W, MODE>, tp);
+}
+
+template <int MODE>
+cudaError_t launch_bulk_table_mode(const BulkTableParams &tp, int W, cudaStream_t stream)
+{
+    switch (W) {
+    case 1: return launch_bulk_table_fixed<1, MODE>(tp, stream);
+    case 2: return launch_bulk_table_fixed<2, MODE>(tp, stream);
+    case 3: return launch_bulk_table_fixed<3, MODE>(tp, stream);
+    case 4: return launch_bulk_table_fixed<4, MODE>(tp, stream);
+    case 5: return launch_bulk_table_fixed<5, MODE>(tp, stream);
+    case 6: return launch_bulk_table_fixed<6, MODE>(tp, stream);
+    case 7: return launch_bulk_table_fixed<7, MODE>(tp, stream);
+    default: return launch_bulk_table_fixed<8, MODE>(tp, stream);
+    }
 }
 
 template <int MODE>
@@ -292,6 +437,21 @@ cudaError_t launch_bulk_mode(const LaunchSpec &s, int64_t head, cudaStream_t str
 cudaError_t read_pipeline_timeouts_bulk(unsigned long long *count) { return read_unit_timeouts(count); }
 
 int bulk_tile_floats(int W) { return W <= 4 ? BulkShape<4>::T : BulkShape<8>::T; }
+
+cudaError_t launch_bulk_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
+                              float scale, int do_scale, int mode, cudaStream_t stream)
+{
+    BulkTableParams tp = {};
+    tp.table = d_table;
+    tp.out = out;
+    tp.status = d_status;
+    tp.len = len;
+    tp.scale = scale;
+    tp.do_scale = do_scale;
+    tp.pdl = DETFOLD_PDL_ALL ? 1 : 0;
+    if (mode == kAllReduce) return launch_bulk_table_mode<kAllReduce>(tp, W, stream);
+    return launch_bulk_table_mode<kSumCoherent>(tp, W, stream);
+}
 
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream)
 {

@@ -51,13 +51,16 @@ PHASE_PLANS = {
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 8])
-@pytest.mark.parametrize("n", [1, 9, 1034, 4099, 65536 + 3, 1 << 17, (1 << 17) + 1])
+@pytest.mark.parametrize("n", [1, 9, 1034, 4099, 65536 + 3, 1 << 17, (1 << 17) + 1,
+                               (1 << 20) + 7, (1 << 21) + 2047])
 @pytest.mark.parametrize("plan", sorted(PHASE_PLANS))
 def test_table_access_widths_heads_and_tails(W, n, plan):
     # The table kernels choose the access width on the device from the
     # entries' phases; every width, with heads and tails, on both sides of
-    # the small-payload bound (2^17 elements), for the sum, the in-place sum
-    # and the all-reduce.
+    # the small-payload bound (2^17 elements) and past the bulk bound (2^20,
+    # where one 16-byte phase runs the bulk pipeline fed from the table and
+    # mixed phases a scalar fold), for the sum, the in-place sum and the
+    # all-reduce.
     rows = gen.stress_rows(W, n)
     offs = [PHASE_PLANS[plan](r) for r in range(W)]
     srcs = [Guarded(n, offs[r], rows[r]) for r in range(W)]

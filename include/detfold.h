@@ -45,6 +45,14 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden symbol visibility; only the entry points
+ * declared here are exported. */
+#if defined(__GNUC__)
+#define DETFOLD_API __attribute__((visibility("default")))
+#else
+#define DETFOLD_API
+#endif
+
 #define DETFOLD_MAX_W 256
 /* Largest accepted len: 2^40 elements (4 TiB per addend). */
 #define DETFOLD_MAX_LEN ((int64_t)1 << 40)
@@ -75,7 +83,7 @@ extern "C" {
  *   out must not overlap stacked (DETFOLD_ERR_OVERLAP).
  * W == 1 copies row 0 into out.
  */
-int detfold_sum_stacked(float *out, const float *stacked, int W, int64_t len, void *stream);
+DETFOLD_API int detfold_sum_stacked(float *out, const float *stacked, int W, int64_t len, void *stream);
 
 /*
  * Pointer-table fold: the same chain over W independent arenas, without the
@@ -89,7 +97,7 @@ int detfold_sum_stacked(float *out, const float *stacked, int W, int64_t len, vo
  *        each other (they are only read).
  *   srcs host array of W device pointers, each to len f32, read.
  */
-int detfold_sum_ptrs(float *out, const float *const *srcs, int W, int64_t len, void *stream);
+DETFOLD_API int detfold_sum_ptrs(float *out, const float *const *srcs, int W, int64_t len, void *stream);
 
 /*
  * The mean as its own pass (mamba-rs src/dist/reducer.rs, module doc: the
@@ -97,7 +105,7 @@ int detfold_sum_ptrs(float *out, const float *const *srcs, int W, int64_t len, v
  *   buf device, len f32, read and written.
  * scale == 1.0f enqueues nothing.
  */
-int detfold_scale(float *buf, int64_t len, float scale, void *stream);
+DETFOLD_API int detfold_scale(float *buf, int64_t len, float scale, void *stream);
 
 /*
  * Fused loopback all-reduce, in place: for each i, read arenas[0..W-1][i],
@@ -110,7 +118,7 @@ int detfold_scale(float *buf, int64_t len, float scale, void *stream);
  *          written. Arenas must be pairwise disjoint (DETFOLD_ERR_OVERLAP).
  * W == 1 leaves the arena as it is except for the mean multiply.
  */
-int detfold_loopback_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
+DETFOLD_API int detfold_loopback_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
                                void *stream);
 
 /*
@@ -119,7 +127,7 @@ int detfold_loopback_allreduce(float *const *arenas, int W, int64_t len, float m
  * every row can share its source shard's 32-byte phase. Returns a negative
  * status for invalid len or W.
  */
-int64_t detfold_staged_workspace_bytes(int64_t len, int W);
+DETFOLD_API int64_t detfold_staged_workspace_bytes(int64_t len, int W);
 
 /*
  * Staged loopback all-reduce: the reference's own dataflow on one device
@@ -142,7 +150,7 @@ int64_t detfold_staged_workspace_bytes(int64_t len, int W);
  * Unlike the reference, no stream synchronization happens between owners:
  * the workspace is caller-owned, so stream order alone protects its reuse.
  */
-int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
+DETFOLD_API int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
                                       float mean_scale, int flags, void *workspace,
                                       int64_t workspace_bytes, void *stream);
 
@@ -163,7 +171,7 @@ int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
  *             touched when the call returns before launching (len == 0 or
  *             a host-side error).
  */
-int detfold_sum_ptrs_dev(float *out, const float *const *d_srcs, int W, int64_t len, int *d_status,
+DETFOLD_API int detfold_sum_ptrs_dev(float *out, const float *const *d_srcs, int W, int64_t len, int *d_status,
                          void *stream);
 
 /*
@@ -171,7 +179,7 @@ int detfold_sum_ptrs_dev(float *out, const float *const *d_srcs, int W, int64_t 
  * detfold_loopback_allreduce, with the table read by the kernel; arenas must
  * be pairwise disjoint -- the caller's contract). d_status as above.
  */
-int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, float mean_scale,
+DETFOLD_API int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, float mean_scale,
                                    int *d_status, void *stream);
 
 /*
@@ -214,7 +222,7 @@ int detfold_loopback_allreduce_dev(float *const *d_arenas, int W, int64_t len, f
 #define DETFOLD_ONESHOT_LINK_BYTES (2 * DETFOLD_ONESHOT_MAX_CTAS * 8 + 64)
 #define DETFOLD_ONESHOT_REFUSE_ENTRY 40043
 #define DETFOLD_ONESHOT_REFUSE_EXIT 40044
-int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
+DETFOLD_API int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float mean_scale,
                                void *link, uint64_t epoch, float *stage, int *words,
                                int64_t wait_ns, int drop_rank, int drop_at_exit, void *stream);
 
@@ -227,7 +235,7 @@ int detfold_one_shot_allreduce(float *const *arenas, int W, int64_t len, float m
  *   src   device, len f32, read.
  * 1 <= ndst <= DETFOLD_MAX_W (DETFOLD_ERR_WORLD). One launch reads src once.
  */
-int detfold_broadcast(float *const *dsts, int ndst, const float *src, int64_t len, void *stream);
+DETFOLD_API int detfold_broadcast(float *const *dsts, int ndst, const float *src, int64_t len, void *stream);
 
 /*
  * All-gather, pure byte movement (same test): every output receives the
@@ -240,7 +248,7 @@ int detfold_broadcast(float *const *dsts, int ndst, const float *src, int64_t le
  * With W <= 8 and every pair at one 16-byte phase, one movement launch for
  * all pairs (each part read once); otherwise one launch per part.
  */
-int detfold_all_gather(float *const *outs, int W, const float *const *parts, int64_t span,
+DETFOLD_API int detfold_all_gather(float *const *outs, int W, const float *const *parts, int64_t span,
                        void *stream);
 
 /*
@@ -251,7 +259,7 @@ int detfold_all_gather(float *const *outs, int W, const float *const *parts, int
  *   starts, lens  host arrays of W int64, written.
  * Host only; touches no device.
  */
-int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens);
+DETFOLD_API int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens);
 
 /*
  * Allocation-free staged loopback all-reduce. The sources have no counterpart:
@@ -277,17 +285,17 @@ int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t *lens);
  *   - No cudaMalloc, cudaFree or allocating library routine is called.
  */
 #define DETFOLD_NOALLOC_SCRATCH_BYTES ((int64_t)16 << 20)
-int detfold_loopback_allreduce_staged_noalloc(float *const *arenas, int W, int64_t len,
+DETFOLD_API int detfold_loopback_allreduce_staged_noalloc(float *const *arenas, int W, int64_t len,
                                               float mean_scale, int flags, void *stream);
 
 /* A static, human-readable name for a status code. */
-const char *detfold_status_string(int status);
+DETFOLD_API const char *detfold_status_string(int status);
 
 /*
  * The cudaError_t value of the last DETFOLD_ERR_CUDA returned on the calling
  * thread (0 if none).
  */
-int detfold_last_cuda_error(void);
+DETFOLD_API int detfold_last_cuda_error(void);
 
 /*
  * Number of bounded waits that ran out, since the library was loaded, in the
@@ -298,7 +306,7 @@ int detfold_last_cuda_error(void);
  * synchronizing the device), so it is a diagnostic, not for hot loops.
  *   count  host, written.
  */
-int detfold_pipeline_timeouts(int64_t *count);
+DETFOLD_API int detfold_pipeline_timeouts(int64_t *count);
 
 /*
  * Launch-latency floor probe: enqueues `count` launches of an empty kernel
@@ -306,7 +314,7 @@ int detfold_pipeline_timeouts(int64_t *count);
  * when pdl != 0, exactly as the small-payload fold path launches. Used to
  * measure the floor that a graph of small folds is compared against.
  */
-int detfold_launch_floor(int count, int pdl, void *stream);
+DETFOLD_API int detfold_launch_floor(int count, int pdl, void *stream);
 
 /*
  * Memory round-trip floor probe: enqueues `count` launches of a one-warp
@@ -320,7 +328,7 @@ int detfold_launch_floor(int count, int pdl, void *stream);
  * Errors: NULL pointer -> ERR_NULL; count < 0 -> ERR_ARG; misaligned ->
  * ERR_ALIGN; src and dst overlap -> ERR_OVERLAP.
  */
-int detfold_memory_floor(const float *src, float *dst, int count, int pdl, void *stream);
+DETFOLD_API int detfold_memory_floor(const float *src, float *dst, int count, int pdl, void *stream);
 
 #ifdef __cplusplus
 }

@@ -73,6 +73,15 @@ def test_binding_constants_match_the_header(df):
         assert value(name) == v, name
 
 
+def test_library_exports_only_the_declared_api(df):
+    # built with hidden visibility: the dynamic symbol table holds the
+    # header's entry points and nothing else of the library
+    out = subprocess.run(["nm", "-D", "--defined-only", df.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    defined = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert defined == set(declared_functions()), sorted(defined ^ set(declared_functions()))
+
+
 def test_library_exports_every_declared_symbol(df):
     out = subprocess.run(["nm", "-D", "--defined-only", df.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout

@@ -265,3 +265,20 @@ def test_allreduce_repeat_call():
     S = arenas[0].copy()
     oracle.allreduce(arenas)
     assert np.array_equal(arenas[0].astype(np.float64), 2.0 * S.astype(np.float64))
+
+
+def test_bit_diffs_counts_exactly_the_differing_words():
+    # the bench's checks count words with bit_diffs: it must compare bits, not
+    # values (+0 vs -0 and two NaN payloads differ), and count each word once
+    a = np.arange(1, 1001, dtype=np.float32)
+    b = a.copy()
+    assert oracle.bit_diffs(a, b) == 0
+    b[[0, 17, 999]] = [np.float32(2.0), np.float32(-18.0), np.nextafter(np.float32(1000), np.float32(0))]
+    assert oracle.bit_diffs(a, b) == 3
+    z = np.zeros(4, dtype=np.float32)
+    nz = z.copy()
+    nz[2] = np.float32(-0.0)
+    assert oracle.bit_diffs(z, nz) == 1
+    n1 = np.array([0x7FC00001, 0x7FC00002], dtype=np.uint32).view(np.float32)
+    assert oracle.bit_diffs(n1, n1.copy()) == 0
+    assert oracle.bit_diffs(n1, n1[::-1].copy()) == 2

@@ -20,8 +20,9 @@ L2, so no L2 flush is needed between steps.
 
 Also reported: per-row kernel times from CUDA events on the launching
 stream, the roofline of the dominant kernel, microseconds per call of the
-16 KiB W=2 fold inside a 10,000-node CUDA graph (with the empty-kernel
-and the one-warp memory round-trip floors), an end-to-end figure through the public API with host buffers, SM
+16 KiB W=2 fold inside a 10,000-node CUDA graph (with the empty-kernel,
+the one-warp memory round-trip and the same-launch-shape floors of
+libdetfold_probes), an end-to-end figure through the public API with host buffers, SM
 clocks sampled during the run, a sampled bit-exact check of the bench's own
 outputs against the CPU oracle, and the oracle timed on host cores.
 
@@ -247,8 +248,8 @@ class Workload:
             self.c5_buf[W] = keep
         self.c2 = {n: self.h_c2[n].to(dev) for n in C2_NS}
         self.c2_out = {n: t.empty(n, dtype=t.float32, device=dev) for n in C2_NS}
-        self.scale4 = float(np.float32(1.0) / np.float32(C4_W))
-        self.scale5 = {W: float(np.float32(1.0) / np.float32(W)) for W in C5_WS}
+        self.scale4 = df.detfold_mean_scale(C4_W)
+        self.scale5 = {W: df.detfold_mean_scale(W) for W in C5_WS}
         torch.cuda.synchronize()
 
     def rows(self):
@@ -259,7 +260,7 @@ class Workload:
             ("c3_ptrs", lambda: df.detfold_sum_ptrs(self.c3_out2, self.c3_rows, C3_W, C3_N), 1),
             ("c4_fused", lambda: df.detfold_loopback_allreduce(self.c4f, C4_W, C4_N, self.scale4), 1),
             ("c4_staged", lambda: df.detfold_loopback_allreduce_staged(
-                self.c4s, C4_W, C4_N, self.scale4, 0, self.ws, self.ws_bytes), 3 * C4_W),
+                self.c4s, C4_W, C4_N, self.scale4, self.ws, self.ws_bytes), 3 * C4_W),
         ]
         for W in C5_WS:
             def c5(W=W):
@@ -323,15 +324,57 @@ def verify_samples(oracle, specs: list[dict]) -> dict:
     return res
 
 
+PROBES_LIB = os.path.join(ROOT, "deterministic_fixed_order_gb300", "libdetfold_probes.so")
+
+
+class Probes:
+    """The latency-floor kernels of libdetfold_probes.so (include/detfold_probes.h),
+    a measurement library of its own that the fold library never loads."""
+
+    def __init__(self, path: str = PROBES_LIB):
+        import ctypes
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        self.lib = lib = ctypes.CDLL(path)
+        lib.detfold_probe_launch_floor.argtypes = [I, I, P]
+        lib.detfold_probe_memory_floor.argtypes = [P, P, I, I, P]
+        lib.detfold_probe_same_shape_floor.argtypes = [P, P, P, I64, I, P]
+        for name in ("detfold_probe_launch_floor", "detfold_probe_memory_floor",
+                     "detfold_probe_same_shape_floor", "detfold_probe_last_cuda_error"):
+            getattr(lib, name).restype = I
+
+    @staticmethod
+    def _stream(stream) -> int:
+        import torch
+        return (stream or torch.cuda.current_stream()).cuda_stream
+
+    def _check(self, rc: int, where: str) -> None:
+        if rc != 0:
+            raise RuntimeError(f"{where}: status {rc} (cudaError {self.lib.detfold_probe_last_cuda_error()})")
+
+    def launch_floor(self, count: int, pdl: int = 1, stream=None) -> None:
+        self._check(self.lib.detfold_probe_launch_floor(count, pdl, self._stream(stream)), "launch_floor")
+
+    def memory_floor(self, src, dst, count: int, pdl: int = 1, stream=None) -> None:
+        self._check(self.lib.detfold_probe_memory_floor(src.data_ptr(), dst.data_ptr(), count, pdl,
+                                                        self._stream(stream)), "memory_floor")
+
+    def same_shape_floor(self, out, src0, src1, n: int, count: int, stream=None) -> None:
+        self._check(self.lib.detfold_probe_same_shape_floor(out.data_ptr(), src0.data_ptr(), src1.data_ptr(),
+                                                            n, count, self._stream(stream)),
+                    "same_shape_floor")
+
+
 def graph_us_per_call(torch, df, wl, rounds: int = 5, reps: int = 5) -> dict:
     """Microseconds per call of graphs of GRAPH_NODES back-to-back calls: the
     W=2 fold at each C2 size (pointer table in the kernel parameters, and
-    through a device-resident table), beside three floors -- an empty
-    kernel with and without programmatic dependent launch, and a one-warp
-    load-after-predecessor + store. Every graph is captured first and then
-    timed round-robin (`rounds` x `reps` replays each), so a drift of the
-    GPU's state during the section shifts all of them alike; each figure
-    is the median over its replays."""
+    through a device-resident table), beside the floors of libdetfold_probes
+    -- an empty kernel with and without programmatic dependent launch, a
+    one-warp load-after-predecessor + store, and at each C2 size a kernel of
+    the fold's own launch shape that moves the same bytes without the adds.
+    Every graph is captured first and then timed round-robin (`rounds` x
+    `reps` replays each), so a drift of the GPU's state during the section
+    shifts all of them alike; each figure is the median over its replays."""
+    probes = Probes()
     stream = torch.cuda.Stream()
 
     def capture(fn):
@@ -357,11 +400,15 @@ def graph_us_per_call(torch, df, wl, rounds: int = 5, reps: int = 5) -> dict:
         keep.append(table)
         graphs[(str(n), "us_per_call_device_table")] = capture(rep(lambda n=n, table=table: df.detfold_sum_ptrs_dev(
             wl.c2_out[n], table, 2, n)))
+        so = torch.empty(n, dtype=torch.float32, device=wl.dev)
+        keep.append(so)
+        graphs[(str(n), "same_shape_floor_us")] = capture(lambda n=n, so=so: probes.same_shape_floor(
+            so, wl.c2[n][:n], wl.c2[n][n:], n, GRAPH_NODES))
     pair = torch.zeros(64, device="cuda")
-    graphs[("floors", "empty_pdl")] = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 1))
-    graphs[("floors", "empty_plain")] = capture(lambda: df.detfold_launch_floor(GRAPH_NODES, 0))
-    graphs[("floors", "memory_pdl")] = capture(lambda: df.detfold_memory_floor(pair[:32], pair[32:],
-                                                                              GRAPH_NODES, 1))
+    graphs[("floors", "empty_pdl")] = capture(lambda: probes.launch_floor(GRAPH_NODES, 1))
+    graphs[("floors", "empty_plain")] = capture(lambda: probes.launch_floor(GRAPH_NODES, 0))
+    graphs[("floors", "memory_pdl")] = capture(lambda: probes.memory_floor(pair[:32], pair[32:],
+                                                                          GRAPH_NODES, 1))
     times = {k: [] for k in graphs}
     for _ in range(rounds):
         for k, g in graphs.items():
@@ -378,6 +425,11 @@ def graph_us_per_call(torch, df, wl, rounds: int = 5, reps: int = 5) -> dict:
     for (group, key), ts in times.items():
         res.setdefault(group, {})[key] = round(statistics.median(ts), 3)
     res["floors"]["spread_us"] = round(max(max(v) - min(v) for v in times.values()), 3)
+    for n in C2_NS:
+        r = res[str(n)]
+        r["ratio_to_same_shape_floor"] = round(r["us_per_call"] / r["same_shape_floor_us"], 3)
+        r["ratio_to_memory_floor"] = round(r["us_per_call"] / res["floors"]["memory_pdl"], 3)
+        r["ratio_to_empty_floor"] = round(r["us_per_call"] / res["floors"]["empty_pdl"], 3)
     del graphs
     # the bits after all the replays must equal one fold: every word goes to
     # the oracle leg

@@ -25,10 +25,10 @@ __all__ = [
     "detfold_broadcast", "detfold_all_gather", "detfold_sum_ptrs_dev",
     "detfold_loopback_allreduce_dev", "device_table", "detfold_one_shot_allreduce", "OneShotLink",
     "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
-    "detfold_loopback_allreduce", "detfold_staged_workspace_bytes",
-    "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_noalloc",
-    "detfold_shard_plan", "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
-    "detfold_memory_floor", "STATUS",
+    "detfold_loopback_allreduce", "detfold_mean_scale", "detfold_staged_workspace_bytes",
+    "detfold_loopback_allreduce_staged", "detfold_loopback_allreduce_staged_ex",
+    "detfold_loopback_allreduce_staged_noalloc", "detfold_shard_plan", "detfold_status_string",
+    "detfold_last_cuda_error", "detfold_pipeline_timeouts", "STATUS",
 ]
 
 LIB_PATH = _build.LIB
@@ -70,7 +70,9 @@ lib.detfold_scale.argtypes = [_P, _I64, _F, _P]
 lib.detfold_loopback_allreduce.argtypes = [_P, _INT, _I64, _F, _P]
 lib.detfold_staged_workspace_bytes.argtypes = [_I64, _INT]
 lib.detfold_staged_workspace_bytes.restype = _I64
-lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _INT, _P, _I64, _P]
+lib.detfold_mean_scale.argtypes = [_INT, _P]
+lib.detfold_loopback_allreduce_staged.argtypes = [_P, _INT, _I64, _F, _P, _I64, _P]
+lib.detfold_loopback_allreduce_staged_ex.argtypes = [_P, _INT, _I64, _F, _INT, _P, _I64, _P]
 lib.detfold_loopback_allreduce_staged_noalloc.argtypes = [_P, _INT, _I64, _F, _INT, _P]
 lib.detfold_broadcast.argtypes = [_P, _INT, _P, _I64, _P]
 lib.detfold_sum_ptrs_dev.argtypes = [_P, _P, _INT, _I64, _P, _P]
@@ -82,16 +84,13 @@ lib.detfold_shard_plan.argtypes = [_I64, _INT, _P, _P]
 lib.detfold_status_string.argtypes = [_INT]
 lib.detfold_status_string.restype = ctypes.c_char_p
 lib.detfold_last_cuda_error.argtypes = []
-lib.detfold_launch_floor.argtypes = [_INT, _INT, _P]
-lib.detfold_memory_floor.argtypes = [_P, _P, _INT, _INT, _P]
 lib.detfold_pipeline_timeouts.argtypes = [_P]
 for _name in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
-              "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
-              "detfold_loopback_allreduce_staged_noalloc", "detfold_broadcast",
-              "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
-              "detfold_one_shot_allreduce",
-              "detfold_all_gather", "detfold_shard_plan", "detfold_last_cuda_error", "detfold_launch_floor",
-              "detfold_memory_floor", "detfold_pipeline_timeouts"):
+              "detfold_loopback_allreduce", "detfold_mean_scale", "detfold_loopback_allreduce_staged",
+              "detfold_loopback_allreduce_staged_ex", "detfold_loopback_allreduce_staged_noalloc",
+              "detfold_broadcast", "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
+              "detfold_one_shot_allreduce", "detfold_all_gather", "detfold_shard_plan",
+              "detfold_last_cuda_error", "detfold_pipeline_timeouts"):
     getattr(lib, _name).restype = _INT
 
 
@@ -206,19 +205,30 @@ def status_loopback_allreduce(arenas, W: int, length: int, mean_scale: float = 1
     return lib.detfold_loopback_allreduce(tab, W, length, mean_scale, _stream(stream))
 
 
-def status_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: float, flags: int,
-                                     workspace, workspace_bytes: int, stream=None) -> int:
+def _workspace_ptr(ws, workspace_bytes: int) -> int:
+    if ws is None or isinstance(ws, int):
+        return ws or 0
+    if not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace: expected a contiguous CUDA tensor")
+    if ws.numel() * ws.element_size() < workspace_bytes:
+        raise ValueError("workspace: tensor smaller than workspace_bytes")
+    return ws.data_ptr()
+
+
+def status_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: float, workspace,
+                                     workspace_bytes: int, stream=None) -> int:
     tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
-    ws = workspace
-    if ws is not None and not isinstance(ws, int):
-        torch = _torch or _t()
-        if not ws.is_cuda or not ws.is_contiguous():
-            raise ValueError("workspace: expected a contiguous CUDA tensor")
-        if ws.numel() * ws.element_size() < workspace_bytes:
-            raise ValueError("workspace: tensor smaller than workspace_bytes")
-        ws = ws.data_ptr()
-    return lib.detfold_loopback_allreduce_staged(tab, W, length, mean_scale, flags, ws or 0,
+    return lib.detfold_loopback_allreduce_staged(tab, W, length, mean_scale,
+                                                 _workspace_ptr(workspace, workspace_bytes),
                                                  workspace_bytes, _stream(stream))
+
+
+def status_loopback_allreduce_staged_ex(arenas, W: int, length: int, mean_scale: float, flags: int,
+                                        workspace, workspace_bytes: int, stream=None) -> int:
+    tab = _ptr_array(arenas, length, "arenas") if arenas is not None else None
+    return lib.detfold_loopback_allreduce_staged_ex(tab, W, length, mean_scale, flags,
+                                                    _workspace_ptr(workspace, workspace_bytes),
+                                                    workspace_bytes, _stream(stream))
 
 
 def status_loopback_allreduce_staged_noalloc(arenas, W: int, length: int, mean_scale: float,
@@ -328,12 +338,29 @@ def detfold_staged_workspace_bytes(length: int, W: int) -> int:
     return n
 
 
+def detfold_mean_scale(W: int) -> float:
+    """fl(1/W) in binary32, computed by the library: the mean's multiplier."""
+    out = ctypes.c_float(0.0)
+    _check(lib.detfold_mean_scale(W, ctypes.byref(out)), "detfold_mean_scale")
+    return out.value
+
+
 def detfold_loopback_allreduce_staged(arenas, W: int, length: int, mean_scale: float = 1.0,
-                                      flags: int = 0, workspace=None, workspace_bytes: int = 0,
+                                      workspace=None, workspace_bytes: int = 0,
                                       stream=None) -> None:
-    _check(status_loopback_allreduce_staged(arenas, W, length, mean_scale, flags, workspace,
+    _check(status_loopback_allreduce_staged(arenas, W, length, mean_scale, workspace,
                                             workspace_bytes, stream),
            "detfold_loopback_allreduce_staged")
+
+
+def detfold_loopback_allreduce_staged_ex(arenas, W: int, length: int, mean_scale: float = 1.0,
+                                         flags: int = 0, workspace=None, workspace_bytes: int = 0,
+                                         stream=None) -> None:
+    """The staged all-reduce with the comparator's variants (DETFOLD_STAGED_*
+    flags: reverse delivery, a separate mean pass, copy-engine copies)."""
+    _check(status_loopback_allreduce_staged_ex(arenas, W, length, mean_scale, flags, workspace,
+                                               workspace_bytes, stream),
+           "detfold_loopback_allreduce_staged_ex")
 
 
 def detfold_loopback_allreduce_staged_noalloc(arenas, W: int, length: int,
@@ -435,17 +462,6 @@ def detfold_pipeline_timeouts() -> int:
     return c.value
 
 
-def detfold_launch_floor(count: int, pdl: int = 1, stream=None) -> None:
-    _check(lib.detfold_launch_floor(count, pdl, _stream(stream)), "detfold_launch_floor")
-
-
-def detfold_memory_floor(src, dst, count: int, pdl: int = 1, stream=None) -> None:
-    """`count` one-warp launches, each copying src[0:32] to dst[0:32] after
-    the preceding grid retires."""
-    _check(lib.detfold_memory_floor(_dev_ptr(src, 32, "src"), _dev_ptr(dst, 32, "dst"), count, pdl,
-                                    _stream(stream)), "detfold_memory_floor")
-
-
 # ------------------------------------------------------------------ tensor conveniences
 
 def sum_stacked(stacked, out=None, stream=None):
@@ -469,19 +485,13 @@ def sum_ptrs(srcs, out=None, stream=None):
 
 def loopback_allreduce(arenas, mean: bool = False, stream=None) -> None:
     W = len(arenas)
-    scale = float(_mean_scale(W)) if mean else 1.0
+    scale = detfold_mean_scale(W) if mean else 1.0
     detfold_loopback_allreduce(list(arenas), W, arenas[0].numel(), scale, stream)
 
 
-def _mean_scale(W: int):
-    # fl(1/W) in binary32: a host-side argument value, computed by the caller.
-    import numpy as np
-    return np.float32(1.0) / np.float32(W)
-
-
 def mean_scale(W: int) -> float:
-    """fl(1/W) in binary32, the scale the mean multiplies by."""
-    return float(_mean_scale(W))
+    """fl(1/W) in binary32, the scale the mean multiplies by (from the library)."""
+    return detfold_mean_scale(W)
 
 
 def shard_plan(length: int, W: int):

@@ -84,16 +84,6 @@ int arenas_valid(float *const *arenas, int W, int64_t len)
     return DETFOLD_OK;
 }
 
-__global__ void empty_kernel(int pdl) { detfold::pdl_enter(pdl); }
-
-// One warp: each lane copies one float, loaded only after the preceding
-// grid has retired (the same dependency a fold launch has on its inputs).
-__global__ void copy_warp_kernel(const float *__restrict__ src, float *__restrict__ dst, int pdl)
-{
-    detfold::pdl_enter(pdl);
-    dst[threadIdx.x] = src[threadIdx.x];
-}
-
 }  // namespace
 
 namespace detfold {
@@ -101,40 +91,6 @@ namespace detfold {
 // Records a failed CUDA call for detfold_last_cuda_error (for entry points
 // defined in other translation units).
 int record_cuda_status(cudaError_t e) { return cuda_status(e); }
-
-// `count` launches of a one-warp kernel, with programmatic dependent launch
-// exactly when pdl != 0 (as the small-payload fold path launches).
-template <typename... Params, typename... Args>
-static cudaError_t launch_floor_kernel(void (*kernel)(Params...), int count, int pdl, cudaStream_t stream,
-                                      Args... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(32, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    for (int k = 0; k < count; ++k) {
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-}
-
-cudaError_t launch_empty(int count, int pdl, cudaStream_t stream)
-{
-    return launch_floor_kernel(empty_kernel, count, pdl, stream, pdl);
-}
-
-cudaError_t launch_copy_warp(const float *src, float *dst, int count, int pdl, cudaStream_t stream)
-{
-    return launch_floor_kernel(copy_warp_kernel, count, pdl, stream, src, dst, pdl);
-}
 
 }  // namespace detfold
 
@@ -212,9 +168,26 @@ int64_t detfold_staged_workspace_bytes(int64_t len, int W)
     return ((int64_t)W * staged_row_stride(len, W) + 8) * 4;
 }
 
+int detfold_mean_scale(int W, float *scale)
+{
+    if (!scale) return DETFOLD_ERR_NULL;
+    if (int rc = check_world(W)) return rc;
+    // one IEEE binary32 division, rounded to nearest-even (host SSE / NEON)
+    volatile float w = (float)W;  // W <= 256 converts exactly
+    *scale = 1.0f / w;
+    return DETFOLD_OK;
+}
+
 int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len, float mean_scale,
-                                      int flags, void *workspace, int64_t workspace_bytes,
-                                      void *stream)
+                                      void *workspace, int64_t workspace_bytes, void *stream)
+{
+    return detfold_loopback_allreduce_staged_ex(arenas, W, len, mean_scale, 0, workspace,
+                                                workspace_bytes, stream);
+}
+
+int detfold_loopback_allreduce_staged_ex(float *const *arenas, int W, int64_t len, float mean_scale,
+                                         int flags, void *workspace, int64_t workspace_bytes,
+                                         void *stream)
 {
     if (!arenas) return DETFOLD_ERR_NULL;
     if (int rc = check_world(W)) return rc;
@@ -458,21 +431,6 @@ int detfold_pipeline_timeouts(int64_t *count)
     if (int rc = cuda_status(detfold::read_pipeline_timeouts_move(&b))) return rc;
     *count = (int64_t)(a + b);
     return DETFOLD_OK;
-}
-
-int detfold_launch_floor(int count, int pdl, void *stream)
-{
-    if (count < 0) return DETFOLD_ERR_ARG;
-    return cuda_status(detfold::launch_empty(count, pdl ? 1 : 0, (cudaStream_t)stream));
-}
-
-int detfold_memory_floor(const float *src, float *dst, int count, int pdl, void *stream)
-{
-    if (!src || !dst) return DETFOLD_ERR_NULL;
-    if (count < 0) return DETFOLD_ERR_ARG;
-    if (!aligned4(src) || !aligned4(dst)) return DETFOLD_ERR_ALIGN;
-    if (intersects(src, 32 * sizeof(float), dst, 32 * sizeof(float))) return DETFOLD_ERR_OVERLAP;
-    return cuda_status(detfold::launch_copy_warp(src, dst, count, pdl ? 1 : 0, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -124,6 +124,23 @@ __device__ __forceinline__ void named_sync(int id, int n)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Named barrier of n threads that also ORs one predicate over them: every
+// participant gets the same answer. A group whose members each ran their own
+// bounded wait meets here and takes one verdict, so no member can leave
+// while another still waits at a later barrier for it. Same memory ordering
+// as bar.sync.
+__device__ __forceinline__ bool named_sync_any(int id, int n, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
 // Host side: this translation unit's counter.
 static inline cudaError_t read_unit_timeouts(unsigned long long *count)
 {

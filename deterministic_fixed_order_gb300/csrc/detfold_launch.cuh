@@ -273,8 +273,6 @@ inline cudaError_t launch_mode(const LaunchSpec &s, cudaStream_t stream)
 cudaError_t launch_sum_nc(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_sum_coherent(const LaunchSpec &s, cudaStream_t stream);
 cudaError_t launch_allreduce(const LaunchSpec &s, cudaStream_t stream);
-cudaError_t launch_empty(int count, int pdl, cudaStream_t stream);
-cudaError_t launch_copy_warp(const float *src, float *dst, int count, int pdl, cudaStream_t stream);
 // Fold or all-reduce over a device-resident pointer table (fold_table.cu).
 cudaError_t launch_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
                          float scale, int do_scale, int mode, cudaStream_t stream);

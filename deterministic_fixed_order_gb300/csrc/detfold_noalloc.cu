@@ -62,6 +62,6 @@ extern "C" int detfold_loopback_allreduce_staged_noalloc(float *const *arenas, i
         if (need > DETFOLD_NOALLOC_SCRATCH_BYTES) return DETFOLD_ERR_SCRATCH_LIMIT;
         if (int rc = scratch_address(&ws)) return rc;
     }
-    return detfold_loopback_allreduce_staged(arenas, W, len, mean_scale, flags, ws,
-                                             DETFOLD_NOALLOC_SCRATCH_BYTES, stream);
+    return detfold_loopback_allreduce_staged_ex(arenas, W, len, mean_scale, flags, ws,
+                                                DETFOLD_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -17,7 +17,9 @@
 // cap). On expiry the kernel counts the event in a device counter that
 // detfold_pipeline_timeouts() reads, waits (bounded) for its own copies in
 // flight, and stops; the call's output is then incomplete and the counter
-// says so.
+// says so. The consumer warps meet at a named barrier after every wait and
+// vote on its outcome (bar.red.or), so they leave together: the second
+// barrier of a tile is reached only by consumers that all passed the first.
 //
 // Preconditions, checked by the dispatcher: W <= 8, every operand at the same
 // 16-byte phase (tiles then start 16-byte aligned), at least one whole tile.
@@ -190,9 +192,13 @@ __device__ __forceinline__ void bulk_run(const BulkParams<W> &p, const BulkSmem<
     long long k = 0;
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
         const int s = (int)(k % S);
-        if (!mbar_wait(&full[s], (uint32_t)((k / S) & 1))) break;
-        if (tc == 0) bulk_wait_read<S - 1>();  // the store of tile k-S has read res[s]
-        named_sync(1, NC);
+        // Each consumer waits (bounded) for the stage itself, which also
+        // makes the bulk copy's bytes visible to it. The vote then gives all
+        // NC consumers one verdict: if any wait ran out, every consumer
+        // leaves the loop here, and none is left at the barrier below.
+        const bool landed = mbar_wait(&full[s], (uint32_t)((k / S) & 1));
+        if (tc == 0 && landed) bulk_wait_read<S - 1>();  // the store of tile k-S has read res[s]
+        if (named_sync_any(1, NC, !landed)) break;
         const float *src = in + (size_t)s * W * T;
         float *dst = res + (size_t)s * T;
         for (int j = tc * 4; j < T; j += NC * 4) {

@@ -35,6 +35,11 @@
  *     (mamba-rs src/dist/reducer.rs `DetReduceKernel::launch`, `copy_d2d`).
  *   - W (the world size) must be 1 <= W <= DETFOLD_MAX_W
  *     (`reduce_sum_reference` asserts a non-empty world).
+ *   - Per device, the library caches what it looks up once: kernel
+ *     attributes, resident-CTA counts and the address of its static scratch
+ *     array. Do not reset a device (cudaDeviceReset) or otherwise replace its
+ *     primary context while the library is in use in the process: later
+ *     calls would use the cached values of the old context.
  */
 #ifndef DETFOLD_H
 #define DETFOLD_H
@@ -69,7 +74,7 @@ extern "C" {
 #define DETFOLD_ERR_ARG (-8)       /* another invalid argument (unknown flag bits)   */
 #define DETFOLD_ERR_SCRATCH_LIMIT (-9) /* request needs more than the static scratch  */
 
-/* Flags of detfold_loopback_allreduce_staged. */
+/* Flags of detfold_loopback_allreduce_staged_ex. */
 #define DETFOLD_STAGED_REVERSE_DELIVERY 1 /* copy peers into the stack in descending rank order */
 #define DETFOLD_STAGED_SEPARATE_SCALE 2   /* mean multiply as its own pass, not in the fold store */
 #define DETFOLD_STAGED_CE_COPIES 4        /* move bytes with cudaMemcpyAsync (copy engines), as the
@@ -122,10 +127,19 @@ DETFOLD_API int detfold_loopback_allreduce(float *const *arenas, int W, int64_t 
                                void *stream);
 
 /*
- * Bytes of device workspace that detfold_loopback_allreduce_staged needs
- * for (len, W): W stack rows of the largest owner shard, padded so that
- * every row can share its source shard's 32-byte phase. Returns a negative
- * status for invalid len or W.
+ * The mean's scale (mamba-rs src/dist/reducer.rs, module doc: the sum is
+ * multiplied by 1/W): *scale = fl(1/W), the binary32 reciprocal of W rounded
+ * to nearest-even, exact for power-of-two W. Pass it as mean_scale.
+ *   scale  host, written.
+ * Host only; touches no device.
+ */
+DETFOLD_API int detfold_mean_scale(int W, float *scale);
+
+/*
+ * Library plumbing (the pages have no counterpart): bytes of device
+ * workspace that the staged all-reduce needs for (len, W) -- W stack rows
+ * of the largest owner shard, padded so that every row can share its source
+ * shard's 32-byte phase. Returns a negative status for invalid len or W.
  */
 DETFOLD_API int64_t detfold_staged_workspace_bytes(int64_t len, int W);
 
@@ -134,15 +148,12 @@ DETFOLD_API int64_t detfold_staged_workspace_bytes(int64_t len, int W);
  * (mamba-rs src/dist/reducer.rs, `LoopbackWorld::run_round`), kept as the
  * comparator of the fused call. For each owner o with a non-empty shard
  * (detfold_shard_plan): copy every rank's slice of that shard into stack
- * slot = source rank (ascending rank order, or descending with
- * DETFOLD_STAGED_REVERSE_DELIVERY -- the bits must not change), fold the
- * slots into arena o's shard, and apply mean_scale in the fold's store (or
- * as a separate pass with DETFOLD_STAGED_SEPARATE_SCALE). Then copy every
+ * slot = source rank, in ascending rank order, fold the slots into arena
+ * o's shard, and apply mean_scale in the fold's store. Then copy every
  * owner's shard to all other arenas. The copies are pure byte movement: one
- * SM movement launch per phase and owner by default (the distribute phase
- * reads the owner's shard once for its W-1 destinations), or one
- * cudaMemcpyAsync per copy with DETFOLD_STAGED_CE_COPIES. Same end state
- * and bits as detfold_loopback_allreduce.
+ * SM movement launch per phase and owner (the distribute phase reads the
+ * owner's shard once for its W-1 destinations). Same end state and bits as
+ * detfold_loopback_allreduce.
  *   arenas    host array of W device pointers (as above, pairwise disjoint).
  *   workspace device, >= detfold_staged_workspace_bytes(len, W) bytes,
  *             16-byte aligned, disjoint from every arena; contents on entry
@@ -151,8 +162,25 @@ DETFOLD_API int64_t detfold_staged_workspace_bytes(int64_t len, int W);
  * the workspace is caller-owned, so stream order alone protects its reuse.
  */
 DETFOLD_API int detfold_loopback_allreduce_staged(float *const *arenas, int W, int64_t len,
-                                      float mean_scale, int flags, void *workspace,
-                                      int64_t workspace_bytes, void *stream);
+                                      float mean_scale, void *workspace, int64_t workspace_bytes,
+                                      void *stream);
+
+/*
+ * The staged all-reduce with the comparator's variants selected by `flags`
+ * (DETFOLD_STAGED_* bits; flags == 0 is detfold_loopback_allreduce_staged):
+ *   DETFOLD_STAGED_REVERSE_DELIVERY  copy the peers into the stack in
+ *       descending rank order -- the slot, not the arrival order, fixes the
+ *       chain, so the bits must not change (the page's delivery-order
+ *       argument for `run_round`);
+ *   DETFOLD_STAGED_SEPARATE_SCALE    the mean multiply as its own pass after
+ *       each owner's fold, as the reference's caller applies it;
+ *   DETFOLD_STAGED_CE_COPIES         move bytes with one cudaMemcpyAsync per
+ *       copy (the copy engines), as the reference's `copy_d2d` does.
+ * Any other bit is DETFOLD_ERR_ARG.
+ */
+DETFOLD_API int detfold_loopback_allreduce_staged_ex(float *const *arenas, int W, int64_t len,
+                                         float mean_scale, int flags, void *workspace,
+                                         int64_t workspace_bytes, void *stream);
 
 /*
  * Pointer-table fold with the table in device memory. The kernel reads the
@@ -268,8 +296,8 @@ DETFOLD_API int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t 
  * is not permitted there), and runtimes whose device memory is owned and
  * budgeted by their own allocator or reserved up front, where a stray
  * allocation would fail or break the budget. It computes exactly what
- * detfold_loopback_allreduce_staged computes, with the same arguments except
- * the workspace: its scratch is a file-scope device array of
+ * detfold_loopback_allreduce_staged_ex computes, with the same arguments
+ * except the workspace: its scratch is a file-scope device array of
  * DETFOLD_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
  * that loads the library holds until the process exits.
  *   - Requests whose workspace (detfold_staged_workspace_bytes(len, W)) is
@@ -288,47 +316,27 @@ DETFOLD_API int detfold_shard_plan(int64_t len, int W, int64_t *starts, int64_t 
 DETFOLD_API int detfold_loopback_allreduce_staged_noalloc(float *const *arenas, int W, int64_t len,
                                               float mean_scale, int flags, void *stream);
 
-/* A static, human-readable name for a status code. */
+/* Library plumbing (no counterpart on the pages): a static, human-readable
+ * name for a status code. */
 DETFOLD_API const char *detfold_status_string(int status);
 
 /*
- * The cudaError_t value of the last DETFOLD_ERR_CUDA returned on the calling
- * thread (0 if none).
+ * Library plumbing (no counterpart on the pages): the cudaError_t value of
+ * the last DETFOLD_ERR_CUDA returned on the calling thread (0 if none).
  */
 DETFOLD_API int detfold_last_cuda_error(void);
 
 /*
- * Number of bounded waits that ran out, since the library was loaded, in the
- * bulk-async (TMA) staged bandwidth path that large aligned folds and
- * all-reduces use (W <= 8, len >= 2^20). Each such wait stops its CTA early,
- * so any nonzero count means some output is incomplete. It should always be
- * 0; tests check that. Synchronous: it reads a device counter (implicitly
- * synchronizing the device), so it is a diagnostic, not for hot loops.
+ * Library plumbing (no counterpart on the pages): number of bounded waits
+ * that ran out, since the library was loaded, in the bulk-async (TMA)
+ * pipelines that large aligned folds, all-reduces and moves use (W <= 8,
+ * len >= 2^20). Each such wait stops its CTA early, so any nonzero count
+ * means some output is incomplete. It should always be 0; tests check that.
+ * Synchronous: it reads a device counter (implicitly synchronizing the
+ * device), so it is a diagnostic, not for hot loops.
  *   count  host, written.
  */
 DETFOLD_API int detfold_pipeline_timeouts(int64_t *count);
-
-/*
- * Launch-latency floor probe: enqueues `count` launches of an empty kernel
- * (one CTA of 32 threads) on `stream`, with programmatic dependent launch
- * when pdl != 0, exactly as the small-payload fold path launches. Used to
- * measure the floor that a graph of small folds is compared against.
- */
-DETFOLD_API int detfold_launch_floor(int count, int pdl, void *stream);
-
-/*
- * Memory round-trip floor probe: enqueues `count` launches of a one-warp
- * kernel in which lane t copies src[t] to dst[t] (t < 32), with the load
- * issued only after the preceding grid has retired (programmatic dependent
- * launch when pdl != 0, as detfold_launch_floor). It is the least any
- * launch can take that reads data a predecessor may have written and then
- * writes its own result, so it is the floor a graph of small folds is
- * compared against, beside the empty-kernel floor.
- *   src, dst  device, 32 floats each, 4-byte aligned, disjoint.
- * Errors: NULL pointer -> ERR_NULL; count < 0 -> ERR_ARG; misaligned ->
- * ERR_ALIGN; src and dst overlap -> ERR_OVERLAP.
- */
-DETFOLD_API int detfold_memory_floor(const float *src, float *dst, int count, int pdl, void *stream);
 
 #ifdef __cplusplus
 }

@@ -1,6 +1,6 @@
 """Run one fold row at a chosen size for a few launches (for profiler captures).
 
-    python -m deterministic_fixed_order_gb300.profile_case ROW --len N [--W W] [--launches K] [--offset E]
+    python profile_case.py ROW --len N [--W W] [--launches K] [--offset E]
 
 ROW is one of: stacked, ptrs, allreduce, staged, scale, small. Inputs are
 seeded synthetic data. --offset E starts every operand E elements past an
@@ -15,7 +15,7 @@ import argparse
 import os
 import sys
 
-_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+_ROOT = os.path.dirname(os.path.abspath(__file__))
 if _ROOT not in sys.path:
     sys.path.insert(0, _ROOT)
 
@@ -63,7 +63,7 @@ def main() -> int:
         else:
             nb = df.detfold_staged_workspace_bytes(n, W)
             ws = torch.empty(nb // 4, dtype=torch.float32, device=dev)
-            fn = lambda: df.detfold_loopback_allreduce_staged(arenas, W, n, 0.25, 0, ws, nb)
+            fn = lambda: df.detfold_loopback_allreduce_staged(arenas, W, n, 0.25, ws, nb)
     for _ in range(a.launches):
         fn()
     torch.cuda.synchronize()

@@ -27,7 +27,7 @@ with torch.cuda.graph(g, stream=s):
     df.detfold_sum_stacked(out, st, W, n)            # stacked rows: mismatched phases -> realign
     df.detfold_sum_ptrs(out, [st[r] for r in range(W)], W, n)   # same; ptrs
     df.detfold_loopback_allreduce(arenas, W, n, 0.25)           # bulk all-reduce
-    df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, 0, ws, nb)  # bulk moves + folds
+    df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, ws, nb)  # bulk moves + folds
 for _ in range(2):
     for r in range(W):
         arenas[r].copy_(torch.from_numpy(rows[r]))

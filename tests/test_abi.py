@@ -23,20 +23,91 @@ def df():
     return m
 
 
-def declared_functions():
-    text = open(HEADER).read()
+PROBES_HEADER = os.path.join(ROOT, "include", "detfold_probes.h")
+PROBES_LIB = os.path.join(ROOT, "deterministic_fixed_order_gb300", "libdetfold_probes.so")
+
+# The fold library's exported API, pinned: the hot-path calls of the boundary,
+# the next rows (movement, device tables, one-shot), the allocation-free
+# staged call and the plumbing. A symbol added or removed must show up here.
+EXPORTED_API = {
+    "detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale", "detfold_loopback_allreduce",
+    "detfold_mean_scale", "detfold_staged_workspace_bytes", "detfold_loopback_allreduce_staged",
+    "detfold_loopback_allreduce_staged_ex", "detfold_shard_plan", "detfold_status_string",
+    "detfold_broadcast", "detfold_all_gather", "detfold_sum_ptrs_dev", "detfold_loopback_allreduce_dev",
+    "detfold_one_shot_allreduce", "detfold_loopback_allreduce_staged_noalloc",
+    "detfold_last_cuda_error", "detfold_pipeline_timeouts",
+}
+PROBES_API = {"detfold_probe_launch_floor", "detfold_probe_memory_floor",
+              "detfold_probe_same_shape_floor", "detfold_probe_last_cuda_error"}
+
+
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(detfold_\w+)\s*\(", text)))
 
 
+def declaration(name, header=HEADER):
+    """The parameter list of one declared function, as (type, name) pairs."""
+    text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, name
+    params = []
+    for p in m.group(1).split(","):
+        p = " ".join(p.split())
+        if p == "void":
+            continue
+        typ, nm = re.match(r"(.*?)\s*(\w+)$", p).groups()
+        params.append((typ.replace(" *", "*").replace("* ", "*"), nm))
+    return params
+
+
 def test_header_declares_the_api():
-    names = declared_functions()
-    for want in ("detfold_sum_stacked", "detfold_sum_ptrs", "detfold_scale",
-                 "detfold_loopback_allreduce", "detfold_loopback_allreduce_staged",
-                 "detfold_staged_workspace_bytes", "detfold_shard_plan",
-                 "detfold_status_string", "detfold_last_cuda_error", "detfold_launch_floor",
-                 "detfold_memory_floor"):
-        assert want in names
+    assert set(declared_functions()) == EXPORTED_API
+    assert set(declared_functions(PROBES_HEADER)) == PROBES_API
+
+
+def test_boundary_signatures_follow_the_scope_table():
+    # the calls of the boundary, with the argument order the hot-path scope
+    # gives them: (out, inputs, W, len, ..., stream)
+    assert declaration("detfold_sum_stacked") == [
+        ("float*", "out"), ("const float*", "stacked"), ("int", "W"), ("int64_t", "len"), ("void*", "stream")]
+    assert declaration("detfold_sum_ptrs") == [
+        ("float*", "out"), ("const float*const*", "srcs"), ("int", "W"), ("int64_t", "len"),
+        ("void*", "stream")]
+    assert declaration("detfold_scale") == [
+        ("float*", "buf"), ("int64_t", "len"), ("float", "scale"), ("void*", "stream")]
+    assert declaration("detfold_loopback_allreduce") == [
+        ("float*const*", "arenas"), ("int", "W"), ("int64_t", "len"), ("float", "mean_scale"),
+        ("void*", "stream")]
+    assert declaration("detfold_staged_workspace_bytes") == [("int64_t", "len"), ("int", "W")]
+    assert declaration("detfold_loopback_allreduce_staged") == [
+        ("float*const*", "arenas"), ("int", "W"), ("int64_t", "len"), ("float", "mean_scale"),
+        ("void*", "workspace"), ("int64_t", "workspace_bytes"), ("void*", "stream")]
+    assert declaration("detfold_shard_plan") == [
+        ("int64_t", "len"), ("int", "W"), ("int64_t*", "starts"), ("int64_t*", "lens")]
+    assert declaration("detfold_status_string") == [("int", "status")]
+    assert declaration("detfold_mean_scale") == [("int", "W"), ("float*", "scale")]
+
+
+def test_mean_scale_is_the_binary32_reciprocal(df):
+    # fl(1/W), bit for bit the oracle's (itself pinned against the exact
+    # rounding model), for every legal W; the binding passes it through
+    for W in range(1, 257):
+        got = np.float32(df.detfold_mean_scale(W))
+        assert got.view(np.uint32) == np.float32(oracle.mean_scale(W)).view(np.uint32), W
+        assert df.mean_scale(W) == float(got)
+    out = ctypes.c_float(0.0)
+    assert df.lib.detfold_mean_scale(0, ctypes.byref(out)) == df.STATUS["DETFOLD_ERR_WORLD"]
+    assert df.lib.detfold_mean_scale(257, ctypes.byref(out)) == df.STATUS["DETFOLD_ERR_WORLD"]
+    assert df.lib.detfold_mean_scale(4, None) == df.STATUS["DETFOLD_ERR_NULL"]
+
+
+def test_binding_does_no_method_arithmetic():
+    # the binding marshals arguments: no numerics library, no float math
+    src = open(os.path.join(ROOT, "deterministic_fixed_order_gb300", "__init__.py")).read()
+    assert not re.search(r"^\s*(import numpy|from numpy|import math|from math)", src, re.M)
+    assert "float32(" not in src and "1.0 /" not in src and "1 /" not in src
 
 
 def test_binding_constants_match_the_header(df):
@@ -79,7 +150,14 @@ def test_library_exports_only_the_declared_api(df):
     out = subprocess.run(["nm", "-D", "--defined-only", df.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
     defined = {line.split()[-1] for line in out.splitlines() if line.strip()}
-    assert defined == set(declared_functions()), sorted(defined ^ set(declared_functions()))
+    assert defined == set(declared_functions()) == EXPORTED_API, sorted(defined ^ EXPORTED_API)
+
+
+def test_probes_library_exports_only_its_header():
+    out = subprocess.run(["nm", "-D", "--defined-only", PROBES_LIB], capture_output=True,
+                         text=True, check=True).stdout
+    defined = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert defined == PROBES_API, sorted(defined ^ PROBES_API)
 
 
 def test_library_exports_every_declared_symbol(df):
@@ -93,7 +171,7 @@ def test_library_exports_every_declared_symbol(df):
 
 
 def test_header_compiles_as_c():
-    src = '#include "detfold.h"\nint main(void){return DETFOLD_OK;}\n'
+    src = '#include "detfold.h"\n#include "detfold_probes.h"\nint main(void){return DETFOLD_OK;}\n'
     r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
                         "-x", "c", "-", "-o", os.devnull], input=src, text=True,
                        capture_output=True)
@@ -206,13 +284,18 @@ def test_validation_staged(df):
     ws_need = df.detfold_staged_workspace_bytes(64, 2)
     arenas = _tab(A, A + 4096)
     W_ = A + (1 << 20)
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 8, W_, ws_need, None) == S["DETFOLD_ERR_ARG"]
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, None, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, W_, ws_need - 4, None) == S["DETFOLD_ERR_WORKSPACE"]
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, W_ + 8, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 64, 1.0, 0, A + 64, ws_need, None) == S["DETFOLD_ERR_OVERLAP"]
-    assert L.detfold_loopback_allreduce_staged(_tab(A, A), 2, 64, 1.0, 0, W_, ws_need, None) == S["DETFOLD_ERR_OVERLAP"]
-    assert L.detfold_loopback_allreduce_staged(arenas, 2, 0, 0.5, 0, None, 0, None) == S["DETFOLD_OK"]
+    X = L.detfold_loopback_allreduce_staged_ex
+    assert X(arenas, 2, 64, 1.0, 8, W_, ws_need, None) == S["DETFOLD_ERR_ARG"]
+    assert X(arenas, 2, 64, 1.0, -1, W_, ws_need, None) == S["DETFOLD_ERR_ARG"]
+    for call in (lambda *a: L.detfold_loopback_allreduce_staged(*a[:4], *a[5:]), X):
+        assert call(arenas, 2, 64, 1.0, 0, None, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
+        assert call(arenas, 2, 64, 1.0, 0, W_, ws_need - 4, None) == S["DETFOLD_ERR_WORKSPACE"]
+        assert call(arenas, 2, 64, 1.0, 0, W_ + 8, ws_need, None) == S["DETFOLD_ERR_WORKSPACE"]
+        assert call(arenas, 2, 64, 1.0, 0, A + 64, ws_need, None) == S["DETFOLD_ERR_OVERLAP"]
+        assert call(_tab(A, A), 2, 64, 1.0, 0, W_, ws_need, None) == S["DETFOLD_ERR_OVERLAP"]
+        assert call(None, 2, 64, 1.0, 0, W_, ws_need, None) == S["DETFOLD_ERR_NULL"]
+        assert call(arenas, 0, 64, 1.0, 0, W_, ws_need, None) == S["DETFOLD_ERR_WORLD"]
+        assert call(arenas, 2, 0, 0.5, 0, None, 0, None) == S["DETFOLD_OK"]
 
 
 @no_gpu_only
@@ -285,20 +368,36 @@ def test_validation_one_shot(df):
 
 
 @no_gpu_only
-def test_validation_scale_and_floor(df):
+def test_validation_scale(df):
     L, S = df.lib, df.STATUS
     assert L.detfold_scale(None, 8, 0.5, None) == S["DETFOLD_ERR_NULL"]
     assert L.detfold_scale(A + 1, 8, 0.5, None) == S["DETFOLD_ERR_ALIGN"]
     assert L.detfold_scale(A, -8, 0.5, None) == S["DETFOLD_ERR_LEN"]
     assert L.detfold_scale(A, 8, 1.0, None) == S["DETFOLD_OK"]   # scale 1: nothing enqueued
-    assert L.detfold_launch_floor(-1, 1, None) == S["DETFOLD_ERR_ARG"]
-    assert L.detfold_launch_floor(0, 1, None) == S["DETFOLD_OK"]
-    assert L.detfold_memory_floor(None, A, 1, 1, None) == S["DETFOLD_ERR_NULL"]
-    assert L.detfold_memory_floor(A, None, 1, 1, None) == S["DETFOLD_ERR_NULL"]
-    assert L.detfold_memory_floor(A, A + 128, -1, 1, None) == S["DETFOLD_ERR_ARG"]
-    assert L.detfold_memory_floor(A + 2, A + 128, 1, 1, None) == S["DETFOLD_ERR_ALIGN"]
-    assert L.detfold_memory_floor(A, A + 124, 1, 1, None) == S["DETFOLD_ERR_OVERLAP"]
-    assert L.detfold_memory_floor(A, A + 128, 0, 1, None) == S["DETFOLD_OK"]
+
+
+@no_gpu_only
+def test_validation_probes(df):
+    import bench
+    P, S = bench.Probes().lib, df.STATUS
+    assert P.detfold_probe_launch_floor(-1, 1, None) == S["DETFOLD_ERR_ARG"]
+    assert P.detfold_probe_launch_floor(0, 1, None) == S["DETFOLD_OK"]
+    assert P.detfold_probe_memory_floor(None, A, 1, 1, None) == S["DETFOLD_ERR_NULL"]
+    assert P.detfold_probe_memory_floor(A, None, 1, 1, None) == S["DETFOLD_ERR_NULL"]
+    assert P.detfold_probe_memory_floor(A, A + 128, -1, 1, None) == S["DETFOLD_ERR_ARG"]
+    assert P.detfold_probe_memory_floor(A + 2, A + 128, 1, 1, None) == S["DETFOLD_ERR_ALIGN"]
+    assert P.detfold_probe_memory_floor(A, A + 124, 1, 1, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert P.detfold_probe_memory_floor(A, A + 128, 0, 1, None) == S["DETFOLD_OK"]
+    F = P.detfold_probe_same_shape_floor
+    B, C = A + (1 << 20), A + (2 << 20)
+    assert F(None, B, C, 4096, 1, None) == S["DETFOLD_ERR_NULL"]
+    assert F(A, B, C, 4096, -1, None) == S["DETFOLD_ERR_ARG"]
+    for n in (0, 1000, 4097, 4096 + 512, (1 << 17) + 1024):
+        assert F(A, B, C, n, 1, None) == S["DETFOLD_ERR_LEN"], n
+    assert F(A + 16, B, C, 4096, 1, None) == S["DETFOLD_ERR_ALIGN"]
+    assert F(A, B + 4, C, 4096, 1, None) == S["DETFOLD_ERR_ALIGN"]
+    assert F(A, A + 4096, C, 4096, 1, None) == S["DETFOLD_ERR_OVERLAP"]
+    assert F(A, B, C, 4096, 0, None) == S["DETFOLD_OK"]
 
 
 @no_gpu_only

@@ -119,7 +119,7 @@ def test_bulk_all_gather_and_staged(W):
     for flags in (0, 1, 2):
         for r in range(W):
             arenas[r].t.copy_(torch.from_numpy(rows[r]))
-        df.detfold_loopback_allreduce_staged([a.t for a in arenas], W, n, scale, flags, ws, nb)
+        df.detfold_loopback_allreduce_staged_ex([a.t for a in arenas], W, n, scale, flags, ws, nb)
         torch.cuda.synchronize()
         want = [rows[r].copy() for r in range(W)]
         oracle.allreduce(want, np.float32(scale))

@@ -79,9 +79,9 @@ def _cases():
         k = Case(gen.normal_rows(W, n), [1] * W, n_out=1)
         nb = df.detfold_staged_workspace_bytes(n, W)
         k.ws = torch.empty(max(1, nb // 4), dtype=torch.float32, device="cuda")
-        k.call = lambda: df.detfold_loopback_allreduce_staged([t.t for t in k.ins], W, n,
-                                                               float(oracle.mean_scale(W)), flags,
-                                                               k.ws, nb)
+        k.call = lambda: df.detfold_loopback_allreduce_staged_ex([t.t for t in k.ins], W, n,
+                                                                  float(oracle.mean_scale(W)), flags,
+                                                                  k.ws, nb)
         return k
     c["staged_sm"] = lambda: staged(0, 4, 4 * M + 13)
     c["staged_ce_copies"] = lambda: staged(4, 4, 4 * M + 13)

@@ -55,7 +55,7 @@ def test_every_entry_point_is_deterministic():
     ws = torch.empty(nb // 4, device="cuda")
     for flags in (0, 1, 4, 7):
         _ok(determinism_diff(
-            lambda k: df.detfold_loopback_allreduce_staged(arenas, W, N, scale, flags, ws, nb),
+            lambda k: df.detfold_loopback_allreduce_staged_ex(arenas, W, N, scale, flags, ws, nb),
             lambda k: arenas, reset), f"staged flags={flags}")
     n2 = 4096
     c2 = torch.from_numpy(gen.c1_rows(2, n2)).cuda()
@@ -109,7 +109,7 @@ def test_entry_points_agree_with_each_other():
         if flags is None:
             df.detfold_loopback_allreduce(arenas, W, N, 1.0)
         else:
-            df.detfold_loopback_allreduce_staged(arenas, W, N, 1.0, flags, ws, nb)
+            df.detfold_loopback_allreduce_staged_ex(arenas, W, N, 1.0, flags, ws, nb)
         got[name] = arenas[W - 1].cpu().numpy()
     torch.cuda.synchronize()
     for name, g in got.items():

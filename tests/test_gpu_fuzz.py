@@ -106,7 +106,7 @@ def test_random_case_matches_oracle(case):
         else:
             nb = df.detfold_staged_workspace_bytes(n, W)
             ws = torch.empty(max(1, nb // 4), dtype=torch.float32, device="cuda")
-            df.detfold_loopback_allreduce_staged(ts, W, n, scale, seed % 8, ws, nb)
+            df.detfold_loopback_allreduce_staged_ex(ts, W, n, scale, seed % 8, ws, nb)
         torch.cuda.synchronize()
         want = [rows[r].copy() for r in range(W)]
         oracle.allreduce(want, np.float32(scale))

@@ -59,8 +59,11 @@ def run_allreduce(rows: np.ndarray, scale: float = 1.0, offsets=None, staged_fla
     else:
         nb = df.detfold_staged_workspace_bytes(n, W)
         ws = torch.empty(max(1, nb // 4), dtype=torch.float32, device="cuda")
-        df.detfold_loopback_allreduce_staged([a.t for a in arenas], W, n, scale, staged_flags,
-                                             ws, nb)
+        if staged_flags == 0:  # the plain call of the C ABI
+            df.detfold_loopback_allreduce_staged([a.t for a in arenas], W, n, scale, ws, nb)
+        else:
+            df.detfold_loopback_allreduce_staged_ex([a.t for a in arenas], W, n, scale, staged_flags,
+                                                    ws, nb)
     sync()
     assert all(a.intact() for a in arenas), "guard band overwritten"
     return [a.host() for a in arenas]
@@ -463,7 +466,10 @@ def test_c4_full_size_w4_fused_and_staged_bitwise():
     for flags in (0, df.DETFOLD_STAGED_SEPARATE_SCALE | df.DETFOLD_STAGED_REVERSE_DELIVERY,
                   df.DETFOLD_STAGED_CE_COPIES):
         staged = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
-        df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, flags, ws, nb)
+        if flags == 0:
+            df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, ws, nb)
+        else:
+            df.detfold_loopback_allreduce_staged_ex(staged, W, n, 0.25, flags, ws, nb)
         sync()
         for r in range(W):
             assert_bitwise(staged[r].cpu().numpy(), exp[r], f"C4 staged flags={flags} rank {r}")
@@ -527,12 +533,15 @@ def test_lengths_beyond_int32():
 
 @pytest.mark.parametrize("pdl", [0, 1])
 def test_floor_probes(pdl):
-    # The probes a graph of small folds is compared against: the empty
-    # kernel runs, and the one-warp round trip copies exactly 32 floats.
+    # The probes a graph of small folds is compared against (their own
+    # library): the empty kernel runs, and the one-warp round trip copies
+    # exactly 32 floats.
+    import bench
+    probes = bench.Probes()
     src = Guarded(32, 0, np.arange(1, 33, dtype=np.float32))
     dst = Guarded(32)
-    df.detfold_launch_floor(5, pdl)
-    df.detfold_memory_floor(src.t, dst.t, 5, pdl)
+    probes.launch_floor(5, pdl)
+    probes.memory_floor(src.t, dst.t, 5, pdl)
     sync()
     assert dst.intact() and src.intact()
     assert_bitwise(dst.host(), np.arange(1, 33, dtype=np.float32), "memory floor copy")
@@ -541,12 +550,30 @@ def test_floor_probes(pdl):
     dst.t.zero_()
     sync()
     with torch.cuda.graph(g, stream=stream):
-        df.detfold_launch_floor(20, pdl)
-        df.detfold_memory_floor(src.t, dst.t, 20, pdl)
+        probes.launch_floor(20, pdl, stream)
+        probes.memory_floor(src.t, dst.t, 20, pdl, stream)
     g.replay()
     sync()
     assert dst.intact()
     assert_bitwise(dst.host(), np.arange(1, 33, dtype=np.float32), "memory floor copy in a graph")
+
+
+@pytest.mark.parametrize("n", [1024, 4096, 65536, 1 << 17])
+def test_same_shape_floor_probe_moves_the_fold_bytes(n):
+    # the same-launch-shape floor of the small W=2 fold reads both sources
+    # and writes n floats: even elements from src0, odd ones from src1
+    import bench
+    probes = bench.Probes()
+    rows = gen.c1_rows(2, n)
+    s0 = Guarded(n, 0, rows[0])
+    s1 = Guarded(n, 0, rows[1])
+    out = Guarded(n)
+    probes.same_shape_floor(out.t, s0.t, s1.t, n, 3)
+    sync()
+    want = rows[0].copy()
+    want[1::2] = rows[1][1::2]
+    assert out.intact() and s0.intact() and s1.intact()
+    assert_bitwise(out.host(), want, f"same-shape probe n={n}")
 
 
 def test_binding_enqueues_on_torchs_current_stream():

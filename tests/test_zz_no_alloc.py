@@ -5,7 +5,7 @@ into a CUDA graph, and runtimes whose device memory is owned by their own
 allocator or fixed up front. For them the library keeps its scratch in a
 static device array (DETFOLD_NOALLOC_SCRATCH_BYTES) and the caller passes only
 the arenas. These tests check, through the C ABI, that it gives the same bits
-as detfold_loopback_allreduce_staged with a caller workspace, on two calls in
+as detfold_loopback_allreduce_staged_ex with a caller workspace, on two calls in
 a row (the second call reuses the scratch the first one left behind), and
 that a request too large for the scratch is refused without running.
 This file is collected last so that a run stopping at the first failure has
@@ -35,7 +35,7 @@ def test_noalloc_matches_staged_with_caller_workspace(W, n, flags):
     assert nb <= df.DETFOLD_NOALLOC_SCRATCH_BYTES
     ws = torch.empty(nb // 4, dtype=torch.float32, device="cuda")
     for call in range(2):
-        df.detfold_loopback_allreduce_staged([a.t for a in ref], W, n, scale, flags, ws, nb)
+        df.detfold_loopback_allreduce_staged_ex([a.t for a in ref], W, n, scale, flags, ws, nb)
         df.detfold_loopback_allreduce_staged_noalloc([a.t for a in new], W, n, scale, flags)
         torch.cuda.synchronize()
         for r in range(W):

@@ -14,10 +14,12 @@
 //   fold_vec_kernel       W <= 8, every operand at one 32- or 16-byte phase:
 //                         scalar head, vector body (all loads of a group
 //                         issued before any add), scalar tail;
-//   fold_realign_kernel   sums whose sources sit at different 4-byte phases:
-//                         vectors on the output's grid, straddles rebuilt
-//                         with warp shuffles;
-//   fold_scalar_kernel    the all-reduce at mismatched phases;
+//   fold_realign_kernel   operands at different 4-byte phases: vectors on
+//                         one reference grid, straddles rebuilt with warp
+//                         shuffles (the all-reduce also assembles each
+//                         arena's aligned stores from two lanes' results);
+//   fold_scalar_kernel    the all-reduce at mismatched phases when
+//                         DETFOLD_AR_REALIGN is 0;
 //   fold_vec/scalar_generic_kernel   8 < W <= 256.
 // Large aligned calls take the bulk-async (TMA) kernels of fold_bulk.cu;
 // device-resident pointer tables take fold_table.cu.
@@ -28,7 +30,8 @@
 //   kSumCoherent  the same with ordinary loads (out may equal one source:
 //                 the in-place fold).
 //   kAllReduce    every arena <- fold(arenas); ordinary loads, then W stores
-//                 (each element is read, then written, by the same thread).
+//                 (each element is read, then written, by the same thread --
+//                 by the same warp in the realigned kernel).
 //
 // Every launch uses programmatic dependent launch: a kernel executes
 // `griddepcontrol.wait` before its first load (its inputs may come from the
@@ -85,11 +88,29 @@
 #ifndef DETFOLD_USE_BULK
 #define DETFOLD_USE_BULK 1  // bulk-async (TMA) staged path for large aligned calls
 #endif
+#ifndef DETFOLD_AR_REALIGN
+#define DETFOLD_AR_REALIGN 1  // all-reduce at mismatched phases: realigned vectors (0: scalar kernel)
+#endif
+#ifndef DETFOLD_REALIGN_THREADS
+#define DETFOLD_REALIGN_THREADS 256  // CTA size of the realigned kernel
+#endif
+#ifndef DETFOLD_REALIGN_U
+#define DETFOLD_REALIGN_U 1  // warp passes per iteration of the realigned kernel (loads issued together)
+#endif
+#ifndef DETFOLD_REALIGN_AR_NOALLOC
+#define DETFOLD_REALIGN_AR_NOALLOC 0  // 1: the realigned kernel's coherent loads skip L1
+#endif
 #ifndef DETFOLD_USE_BULK_MOVE
 #define DETFOLD_USE_BULK_MOVE 1  // bulk-async path for large pure-movement launches
 #endif
 #ifndef DETFOLD_BULK_MIN_LEN
-#define DETFOLD_BULK_MIN_LEN (1 << 20)  // elements at or above: the bulk path
+#define DETFOLD_BULK_MIN_LEN (1 << 21)  // elements at or above: the bulk path (folds, parameter table)
+#endif
+#ifndef DETFOLD_BULK_TABLE_MIN_LEN
+#define DETFOLD_BULK_TABLE_MIN_LEN (1 << 20)  // the same for folds over a device-resident table
+#endif
+#ifndef DETFOLD_BULK_MOVE_MIN_LEN
+#define DETFOLD_BULK_MOVE_MIN_LEN (1 << 20)  // the same for pure-movement launches
 #endif
 #ifndef DETFOLD_SMALL_PDL
 #define DETFOLD_SMALL_PDL 1  // programmatic dependent launch on the small path
@@ -496,15 +517,27 @@ __global__ void __launch_bounds__(max_threads<MODE>()) fold_scalar_generic_kerne
 
 // ---------------------------------------------------------------- realigned vector kernel
 
-// Sum modes with sources at different 4-byte phases (e.g. the rows of a
-// [W][len] stack when len % 8 != 0). Vectors follow the output's 32-byte
-// alignment; source r's eight elements of output vector v straddle two
-// aligned 32-byte vectors, at element shift d_r = phase of (src_r + head).
-// Each lane loads one aligned vector per source; the upper half of its
-// straddle is the next lane's vector, taken with a warp shuffle. A warp
-// therefore produces 31 output vectors per pass: lane 31 only loads, to feed
-// lane 30. The body covers output vectors 1 .. nvec-2 (loads 1 .. nvec-1),
-// which keeps every load inside every source; the edges are scalar.
+// Operands at different 4-byte phases (e.g. the rows of a [W][len] stack
+// when len % 8 != 0, or arenas at per-rank offsets). Logical vectors of 8
+// elements follow one reference 32-byte grid: the output's for the sums,
+// arena 0's for the all-reduce. Operand r's eight elements of logical vector
+// v straddle two of its aligned 32-byte vectors, at element shift d_r =
+// phase of (src_r + head). Each lane loads one aligned vector per operand;
+// the upper half of its straddle is the next lane's vector, taken with a
+// warp shuffle. A warp therefore folds 31 logical vectors per pass: lane 31
+// only loads, to feed lane 30. The body covers logical vectors 1 .. nvec-2
+// (loads 1 .. nvec-1), which keeps every load inside every operand; the
+// edges are scalar.
+//
+// The all-reduce stores the mirror image: the aligned vector a lane loaded
+// from arena r holds the last d_r elements of logical vector v-1 (folded by
+// the previous lane, taken with an upward shuffle) and the first 8-d_r of
+// v (its own). A lane stores it whole when the pass folded both; at a pass's
+// two ends it stores only the elements the pass folded, one by one. So every
+// element is written once, by the pass that folded it, and a pass uses only
+// elements that no other pass writes: the other elements of the vectors it
+// loads at its ends are loaded but never used, and the update in place needs
+// no ordering between passes.
 template <int NT>
 struct RealignParams {
     const float *src[NT];
@@ -516,10 +549,16 @@ struct RealignParams {
     int pdl;
 };
 
+// Realigned kernel loads. They allocate in L1 (the vector at a pass's end
+// is loaded again by the next pass), except in the coherent modes (in-place
+// fold, all-reduce) when DETFOLD_REALIGN_AR_NOALLOC is set. NC: the
+// read-only path.
 template <bool NC>
 __device__ __forceinline__ Vec<8> ldv8_l1(const float *p)
 {
     Vec<8> r;
+    if constexpr (!NC && DETFOLD_REALIGN_AR_NOALLOC)
+        return ldv<8, false>(p);
     if constexpr (NC)
         asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                      : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
@@ -542,86 +581,133 @@ __device__ __forceinline__ Vec<8> take8(const Vec<8> &a, const Vec<8> &b)
     return x;
 }
 
-template <int W, int MODE>
-__global__ void __launch_bounds__(256) fold_realign_kernel(const __grid_constant__ RealignParams<W> p)
+// x[k] = a[k+D] for k+D < 8, else b[k+D-8], for a warp-uniform runtime D in 0..7.
+__device__ __forceinline__ Vec<8> take8_rt(const Vec<8> &a, const Vec<8> &b, int d)
 {
-    static_assert(MODE != kAllReduce, "all-reduce stores need every arena aligned");
+    switch (d) {
+    case 0: return a;
+    case 1: return take8<1>(a, b);
+    case 2: return take8<2>(a, b);
+    case 3: return take8<3>(a, b);
+    case 4: return take8<4>(a, b);
+    case 5: return take8<5>(a, b);
+    case 6: return take8<6>(a, b);
+    default: return take8<7>(a, b);
+    }
+}
+
+// One pass of a warp over logical vectors v = 1 + 31c + lane, with the
+// lane's aligned vectors of every operand already loaded into lo[].
+template <int W, int MODE>
+__device__ __forceinline__ void realign_pass(const RealignParams<W> &p, const Vec<8> (&lo)[W], int64_t v,
+                                             int lane)
+{
+    const bool writes = lane < 31 && v <= p.nvec - 2;
+    const int64_t e = p.head + v * 8;
+    Vec<8> acc;
+#pragma unroll
+    for (int r = 0; r < W; ++r) {
+        Vec<8> x;
+        const int d = p.shift[r];  // uniform: no divergence
+        if (d == 0) {
+            x = lo[r];
+        } else {
+            Vec<8> hi;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) hi.v[k] = __shfl_down_sync(0xffffffffu, lo[r].v[k], 1);
+            x = take8_rt(lo[r], hi, d);
+        }
+        if (r == 0) {
+            acc = x;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc.v[k] = __fadd_rn(acc.v[k], x.v[k]);
+        }
+    }
+    if (p.do_scale) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc.v[k] = __fmul_rn(acc.v[k], p.scale);
+    }
+    if constexpr (MODE == kAllReduce) {
+        // the previous lane's result: the head of every arena's aligned
+        // vector at this lane
+        Vec<8> prev;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) prev.v[k] = __shfl_up_sync(0xffffffffu, acc.v[k], 1);
+        const bool own_prev = lane > 0 && v - 1 <= p.nvec - 2;  // logical v-1 folded in this pass
+        const bool own_cur = writes;                            // logical v folded in this pass
+#pragma unroll
+        for (int r = 0; r < W; ++r) {
+            const int d = p.shift[r];
+            float *dst = const_cast<float *>(p.src[r]) + e - d;  // the aligned vector loaded
+            if (d == 0) {
+                if (own_cur) stv<8>(dst, acc);
+            } else if (own_prev || own_cur) {
+                const Vec<8> x = take8_rt(prev, acc, 8 - d);  // x[m] = prev[8-d+m] (m < d), acc[m-d]
+                if (own_prev && own_cur) {
+                    stv<8>(dst, x);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        if (m < d ? own_prev : own_cur) st1(dst + m, x.v[m]);
+                }
+            }
+        }
+    } else if (writes) {
+        stv<8>(p.out + e, acc);
+    }
+}
+
+// A warp runs DETFOLD_REALIGN_U passes per iteration (passes c, c + nwarps,
+// ...), with the loads of all of them issued before the first pass's
+// shuffles, so more bytes are in flight per thread.
+template <int W, int MODE>
+__global__ void __launch_bounds__(DETFOLD_REALIGN_THREADS) fold_realign_kernel(const __grid_constant__ RealignParams<W> p)
+{
     constexpr bool NC = (MODE == kSumNC);
+    constexpr int U = DETFOLD_REALIGN_U;
     pdl_enter(p.pdl);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = stride >> 5;
     // warp-uniform loop: every lane of a warp runs every pass (for the shuffles)
-    for (int64_t c = gtid >> 5; 1 + c * 31 < p.nvec - 1; c += nwarps) {
-        const int64_t v = 1 + c * 31 + lane;
-        const bool loads = v <= p.nvec - 1;
-        const bool writes = lane < 31 && v <= p.nvec - 2;
-        const int64_t e = p.head + v * 8;
-        Vec<8> lo[W];
+    for (int64_t c = gtid >> 5; 1 + c * 31 < p.nvec - 1; c += U * nwarps) {
+        Vec<8> lo[U][W];
 #pragma unroll
-        for (int r = 0; r < W; ++r) {
-            if (loads) {
-                lo[r] = ldv8_l1<NC>(p.src[r] + e - p.shift[r]);
-            } else {
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = 1 + (c + u * nwarps) * 31 + lane;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) lo[r].v[k] = 0.0f;
-            }
-        }
-        Vec<8> acc;
+            for (int r = 0; r < W; ++r) {
+                if (v <= p.nvec - 1) {
+                    lo[u][r] = ldv8_l1<NC>(p.src[r] + p.head + v * 8 - p.shift[r]);
+                } else {
 #pragma unroll
-        for (int r = 0; r < W; ++r) {
-            Vec<8> x;
-            const int d = p.shift[r];  // uniform: no divergence
-            if (d == 0) {
-                x = lo[r];
-            } else {
-                Vec<8> hi;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) hi.v[k] = __shfl_down_sync(0xffffffffu, lo[r].v[k], 1);
-                switch (d) {
-                case 1: x = take8<1>(lo[r], hi); break;
-                case 2: x = take8<2>(lo[r], hi); break;
-                case 3: x = take8<3>(lo[r], hi); break;
-                case 4: x = take8<4>(lo[r], hi); break;
-                case 5: x = take8<5>(lo[r], hi); break;
-                case 6: x = take8<6>(lo[r], hi); break;
-                default: x = take8<7>(lo[r], hi); break;
+                    for (int k = 0; k < 8; ++k) lo[u][r].v[k] = 0.0f;
                 }
             }
-            if (r == 0) {
-                acc = x;
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) acc.v[k] = __fadd_rn(acc.v[k], x.v[k]);
-            }
         }
-        if (writes) {
-            if (p.do_scale) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) acc.v[k] = __fmul_rn(acc.v[k], p.scale);
-            }
-            stv<8>(p.out + e, acc);
-        }
+        for (int u = 0; u < U; ++u) realign_pass<W, MODE>(p, lo[u], 1 + (c + u * nwarps) * 31 + lane, lane);
     }
     // scalar edges: [0, lo_end) and [hi_begin, len), disjoint from the body
     // and from each other
     const int64_t body = p.nvec >= 3 ? p.nvec - 2 : 0;
     const int64_t lo_end = body ? p.head + 8 : p.len;
     const int64_t hi_begin = body ? p.head + 8 * (p.nvec - 1) : p.len;
-    for (int64_t i = gtid; i < lo_end; i += stride) {
-        float acc = ld1<NC>(p.src[0] + i);
+    for (int part = 0; part < 2; ++part) {
+        for (int64_t i = (part ? hi_begin : 0) + gtid; i < (part ? p.len : lo_end); i += stride) {
+            float acc = ld1<NC>(p.src[0] + i);
 #pragma unroll
-        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
-        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
-        st1(p.out + i, acc);
-    }
-    for (int64_t i = hi_begin + gtid; i < p.len; i += stride) {
-        float acc = ld1<NC>(p.src[0] + i);
+            for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
+            if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+            if constexpr (MODE == kAllReduce) {
 #pragma unroll
-        for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<NC>(p.src[r] + i));
-        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
-        st1(p.out + i, acc);
+                for (int r = 0; r < W; ++r) st1(const_cast<float *>(p.src[r]) + i, acc);
+            } else {
+                st1(p.out + i, acc);
+            }
+        }
     }
 }
 

@@ -2,8 +2,8 @@
 // planning (vector width, head, body, tail), grid sizing, the typed launch
 // of one kernel instantiation, and the dispatch order of a fold call:
 // bulk-async path (large, aligned, W <= 8) -> small-payload kernel (small,
-// common phase) -> vector kernel (common phase) -> realigned vectors (sums at
-// mismatched phases) -> scalar kernel.
+// common phase) -> vector kernel (common phase) -> realigned vectors
+// (mismatched phases).
 #pragma once
 
 #include <atomic>
@@ -214,10 +214,11 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         constexpr int VT = vec_threads<W, 4, U, MODE>();
         return launch_kernel<fold_vec_kernel<W, 4, U, MODE>>(p, pl.nvec, U, small, VT, C * (T / VT), stream);
     }
-    if constexpr (MODE != kAllReduce) {
-        // no common phase: realign every source onto the output's 32-byte grid
+    if (MODE != kAllReduce || DETFOLD_AR_REALIGN) {
+        // no common phase: realign every operand onto one 32-byte grid, the
+        // output's for a sum, arena 0's for the all-reduce
         RealignParams<W> q = {};
-        const int ph = elem_phase(s.out, 8);
+        const int ph = elem_phase(MODE == kAllReduce ? (const void *)s.src[0] : (const void *)s.out, 8);
         q.head = (8 - ph) % 8;
         if (q.head > s.len) q.head = s.len;
         q.nvec = (s.len - q.head) / 8;
@@ -230,13 +231,14 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         q.scale = s.scale;
         q.do_scale = s.do_scale;
         q.pdl = p.pdl;
-        // a warp covers 31 vectors per pass
+        // a warp covers 31 vectors per pass, DETFOLD_REALIGN_U passes per iteration
         const int64_t work = q.nvec > 2 ? (q.nvec - 2 + 30) / 31 * 32 : 32;
-        return launch_kernel<fold_realign_kernel<W, MODE>>(q, work, 1, small, 256, 0, stream);
-    } else {
-        constexpr int U = u_for<MODE>(W, 0);
-        return launch_kernel<fold_scalar_kernel<W, U, MODE>>(p, s.len, U, small, T, C, stream);
+        static_assert(DETFOLD_SMALL_THREADS <= DETFOLD_REALIGN_THREADS, "small launches fit the launch bound");
+        return launch_kernel<fold_realign_kernel<W, MODE>>(q, work, DETFOLD_REALIGN_U, small,
+                                                           DETFOLD_REALIGN_THREADS, 0, stream);
     }
+    constexpr int U = u_for<MODE>(W, 0);
+    return launch_kernel<fold_scalar_kernel<W, U, MODE>>(p, s.len, U, small, T, C, stream);
 }
 
 template <int MODE>

@@ -339,7 +339,7 @@ cudaError_t launch_table(const float *const *d_table, float *out, int *d_status,
     p.pdl = ((small && DETFOLD_SMALL_PDL) || DETFOLD_PDL_ALL) ? 1 : 0;
     const int64_t work = (len + 7) / 8 > 0 ? (len + 7) / 8 : 1;  // vectors if 32-byte access
     // Bulk-sized calls with W <= 8: the bulk-async pipeline, fed from the table.
-    if (DETFOLD_USE_BULK && !small && W <= 8 && len >= DETFOLD_BULK_MIN_LEN)
+    if (DETFOLD_USE_BULK && !small && W <= 8 && len >= DETFOLD_BULK_TABLE_MIN_LEN)
         return launch_bulk_table(d_table, out, d_status, W, len, scale, do_scale, mode, stream);
     // Small payloads: the register-table kernel (shortest dependent chain;
     // one thread per 32-byte vector). Bandwidth-sized calls: the

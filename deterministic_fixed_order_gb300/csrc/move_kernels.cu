@@ -261,7 +261,7 @@ static cudaError_t launch_move_chunk(const float *const *src, float *const *dst,
                                      int64_t len, cudaStream_t stream)
 {
     // bulk-async path: large, every operand at one 16-byte phase, <= 8 distinct sources
-    if (DETFOLD_USE_BULK && DETFOLD_USE_BULK_MOVE && len >= DETFOLD_BULK_MIN_LEN) {
+    if (DETFOLD_USE_BULK && DETFOLD_USE_BULK_MOVE && len >= DETFOLD_BULK_MOVE_MIN_LEN) {
         int groups = 0;
         for (int k = 0; k < K; ++k) groups += (k == 0 || src[k] != src[k - 1]);
         const int ph = elem_phase_any(src[0], 4);

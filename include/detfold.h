@@ -329,8 +329,10 @@ DETFOLD_API int detfold_last_cuda_error(void);
 /*
  * Library plumbing (no counterpart on the pages): number of bounded waits
  * that ran out, since the library was loaded, in the bulk-async (TMA)
- * pipelines that large aligned folds, all-reduces and moves use (W <= 8,
- * len >= 2^20). Each such wait stops its CTA early, so any nonzero count
+ * pipelines that large aligned folds, all-reduces and moves use (W <= 8;
+ * len >= 2^21 for folds over pointer tables passed from the host, len >= 2^20
+ * for folds over device-resident tables and for moves). Each such wait
+ * stops its CTA early, so any nonzero count
  * means some output is incomplete. It should always be 0; tests check that.
  * Synchronous: it reads a device counter (implicitly synchronizing the
  * device), so it is a diagnostic, not for hot loops.

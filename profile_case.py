@@ -5,7 +5,8 @@
 ROW is one of: stacked, ptrs, allreduce, staged, scale, small. Inputs are
 seeded synthetic data. --offset E starts every operand E elements past an
 allocation boundary (E = 1 is the odd-world stress layout, base + 4 bytes;
-stacked keeps its rows contiguous after the offset). Parity of these calls is
+stacked keeps its rows contiguous after the offset); --mixed adds 3r mod 8
+elements to operand r, so every rank sits at its own 4-byte phase. Parity of these calls is
 established by the test suite; this runner only launches them and reports
 the status.
 """
@@ -27,6 +28,8 @@ def main() -> int:
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--offset", type=int, default=0)
+    ap.add_argument("--mixed", action="store_true",
+                    help="operand r at offset + (3r mod 8) elements: every rank at its own 4-byte phase")
     a = ap.parse_args()
     if not 0 <= a.offset < 64:
         ap.error("--offset must be in [0, 64)")
@@ -43,8 +46,10 @@ def main() -> int:
         flat = torch.empty(W * n + off, dtype=torch.float32, device=dev)
         d = flat[off:].view(W, n)
         d.copy_(torch.from_numpy(rows))
-    else:  # one allocation per operand, each at the offset
-        d = [torch.empty(n + off, dtype=torch.float32, device=dev)[off:] for _ in range(W)]
+    else:  # one allocation per operand, each at the offset (plus its own phase with --mixed)
+        shift = [(3 * r) % 8 if a.mixed else 0 for r in range(W)]
+        d = [torch.empty(n + off + 8, dtype=torch.float32, device=dev)[off + shift[r]:off + shift[r] + n]
+             for r in range(W)]
         for r in range(W):
             d[r].copy_(torch.from_numpy(rows[r]))
     out = torch.empty(n + off, dtype=torch.float32, device=dev)[off:]

@@ -24,7 +24,7 @@ import deterministic_fixed_order_gb300 as df
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
 
-M = 1 << 20
+M = 1 << 21  # the fold's bulk-async threshold (DETFOLD_BULK_MIN_LEN)
 
 
 class Case:

@@ -21,10 +21,13 @@ import deterministic_fixed_order_gb300 as df
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
 
-SMALL, BULK = 1 << 17, 1 << 20
+# the small-payload bound; the bulk-async bounds of table folds and moves
+# (2^20) and of parameter-table folds (2^21)
+SMALL, BULK, BULK2 = 1 << 17, 1 << 20, 1 << 21
 BOUNDARIES = [1, 3, 4, 7, 8, 9, 1023, 1024, 1025, 2047, 2048, 2049, 4096 + 5,
               SMALL - 1, SMALL, SMALL + 1, SMALL + 7,
-              BULK - 1, BULK, BULK + 1, BULK + 7, BULK + 1023, BULK + 2047, BULK + 2048, BULK + 4095]
+              BULK - 1, BULK, BULK + 1, BULK + 7, BULK + 1023, BULK + 2047, BULK + 2048, BULK + 4095,
+              BULK2 - 1, BULK2, BULK2 + 7, BULK2 + 2047, BULK2 + 4095]
 ENTRIES = ["stacked", "ptrs", "in_place", "allreduce", "staged", "table_sum", "table_allreduce",
            "broadcast", "all_gather", "one_shot", "staged_noalloc"]
 

@@ -149,6 +149,26 @@ def test_mismatched_phases(W, n):
         assert_bitwise(got[r], exp[r], f"all-reduce W={W} n={n} rank={r}")
 
 
+@pytest.mark.parametrize("W", [2, 3, 5, 8])
+def test_mixed_phase_allreduce_across_pass_edges(W):
+    # The realigned all-reduce folds 31 logical vectors (248 elements) per
+    # warp pass and stores each arena's aligned vectors whole inside a pass,
+    # element by element at its two ends. Lengths on both sides of several
+    # pass edges, with random per-arena phases, must still give every arena
+    # the oracle's bits, and leave the guard bands intact.
+    rng = np.random.default_rng(7 + W)
+    lengths = sorted({*range(1, 40), *(8 * k + d for k in (31, 62, 93, 155) for d in (-9, -1, 0, 1, 7, 9, 17)),
+                      2047, 4099, 8 * 31 * 64 + 5})
+    for n in lengths:
+        rows = gen.stress_rows(W, n, seed0=int(rng.integers(1, 1 << 30)))
+        offs = [int(x) for x in rng.integers(0, 8, size=W)]
+        scale = float(oracle.mean_scale(W)) if n % 2 else 1.0
+        got = run_allreduce(rows, scale, offs)
+        exp = oracle_allreduce(rows, np.float32(scale))
+        for r in range(W):
+            assert_bitwise(got[r], exp[r], f"mixed-phase all-reduce W={W} n={n} offs={offs} rank={r}")
+
+
 # ------------------------------------------------------------------ C5: odd worlds, stress values
 
 @pytest.mark.parametrize("W", [3, 6])

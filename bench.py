@@ -64,11 +64,11 @@ E2E_PASSES = 5  # end-to-end passes; `e2e.value` is their median
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147581184 + 259530752,
-                                  "kernel_hash": "b29e631b7c2485b5"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147588352 + 259558912,
+                                  "kernel_hash": "2abd361dee919241"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600033024 + 1538559232,
-                                         "kernel_hash": "b29e631b7c2485b5"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600031232 + 1538103296,
+                                         "kernel_hash": "2abd361dee919241"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",

@@ -2,7 +2,9 @@
 
     python profile_case.py ROW --len N [--W W] [--launches K] [--offset E]
 
-ROW is one of: stacked, ptrs, allreduce, staged, scale, small. Inputs are
+ROW is one of: stacked, ptrs, allreduce, staged, scale, small, or torch_add
+(torch's own elementwise add of two operands, W = 2, as a reference for a
+launch of the same size that this library does not run). Inputs are
 seeded synthetic data. --offset E starts every operand E elements past an
 allocation boundary (E = 1 is the odd-world stress layout, base + 4 bytes;
 stacked keeps its rows contiguous after the offset); --mixed adds 3r mod 8
@@ -23,7 +25,7 @@ if _ROOT not in sys.path:
 
 def main() -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("row", choices=["stacked", "ptrs", "allreduce", "staged", "scale", "small"])
+    ap.add_argument("row", choices=["stacked", "ptrs", "allreduce", "staged", "scale", "small", "torch_add"])
     ap.add_argument("--len", type=int, required=True)
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--launches", type=int, default=3)
@@ -58,6 +60,8 @@ def main() -> int:
     elif a.row == "ptrs":
         srcs = [d[r] for r in range(W)]
         fn = lambda: df.detfold_sum_ptrs(out, srcs, W, n)
+    elif a.row == "torch_add":  # reference: torch's own elementwise kernel on the same operands (W = 2)
+        fn = lambda: torch.add(d[0], d[1], out=out)
     elif a.row == "scale":
         out.copy_(d[0])
         fn = lambda: df.detfold_scale(out, n, 0.5)

@@ -221,7 +221,22 @@ class Workload:
             h = pin(2 * n)
             gen.fill_recipe("vecf", h.data_ptr(), 2, n, n)
             self.h_c2[n] = h
-        # device buffers
+        self._device_buffers()
+        self.scale4 = df.detfold_mean_scale(C4_W)
+        self.scale5 = {W: df.detfold_mean_scale(W) for W in C5_WS}
+        torch.cuda.synchronize()
+
+    def device_twin(self):
+        """The same workload (the same host inputs) on a second set of device
+        buffers: the end-to-end leg alternates steps between the two sets."""
+        import copy
+        twin = copy.copy(self)
+        twin._device_buffers()
+        self.torch.cuda.synchronize()
+        return twin
+
+    def _device_buffers(self):
+        t, dev, df = self.torch, self.dev, self.df
         self.c3 = self.h_c3.to(dev)
         self.c3_rows = [self.c3[r * C3_N:(r + 1) * C3_N] for r in range(C3_W)]
         self.c3_out = t.empty(C3_N, dtype=t.float32, device=dev)
@@ -249,9 +264,6 @@ class Workload:
             self.c5_buf[W] = keep
         self.c2 = {n: self.h_c2[n].to(dev) for n in C2_NS}
         self.c2_out = {n: t.empty(n, dtype=t.float32, device=dev) for n in C2_NS}
-        self.scale4 = df.detfold_mean_scale(C4_W)
-        self.scale5 = {W: df.detfold_mean_scale(W) for W in C5_WS}
-        torch.cuda.synchronize()
 
     def rows(self):
         """(name, callable, kernel launches) in step order."""
@@ -899,24 +911,36 @@ def run_gpu(args) -> None:
         h_out[f"c5a{W}"] = pin(W * C5_N)
     for n in C2_NS:
         h_out[f"c2{n}"] = pin(n)
-    # (row name, [(device dst, host src)], [(host dst, device src)])
-    io = {
-        "c3_stacked": ([(wl.c3, wl.h_c3)], [(h_out["c3"], wl.c3_out)]),
-        "c3_ptrs": ([], [(h_out["c3b"], wl.c3_out2)]),
-        "c4_fused": ([(wl.c4f[r], wl.h_c4[r * C4_N:(r + 1) * C4_N]) for r in range(C4_W)],
-                     [(h_out["c4f"][r * C4_N:(r + 1) * C4_N], wl.c4f[r]) for r in range(C4_W)]),
-        "c4_staged": ([(wl.c4s[r], wl.h_c4[r * C4_N:(r + 1) * C4_N]) for r in range(C4_W)],
-                      [(h_out["c4s"][r * C4_N:(r + 1) * C4_N], wl.c4s[r]) for r in range(C4_W)]),
-    }
-    for W in C5_WS:
-        ins, outs = [], [(h_out[f"c5s{W}"], wl.c5_out[W])]
-        for r in range(W):
-            src = wl.h_c5[W][r * C5_N:(r + 1) * C5_N]
-            ins += [(wl.c5_sum_src[W][r], src), (wl.c5_ar[W][r], src)]
-            outs.append((h_out[f"c5a{W}"][r * C5_N:(r + 1) * C5_N], wl.c5_ar[W][r]))
-        io[f"c5_w{W}"] = (ins, outs)
-    for n in C2_NS:
-        io[f"c2_{n}"] = ([(wl.c2[n], wl.h_c2[n])], [(h_out[f"c2{n}"], wl.c2_out[n])])
+    def io_of(w):
+        """(row name -> [(device dst, host src)], [(host dst, device src)]) of
+        one set of device buffers."""
+        io = {
+            "c3_stacked": ([(w.c3, w.h_c3)], [(h_out["c3"], w.c3_out)]),
+            "c3_ptrs": ([], [(h_out["c3b"], w.c3_out2)]),
+            "c4_fused": ([(w.c4f[r], w.h_c4[r * C4_N:(r + 1) * C4_N]) for r in range(C4_W)],
+                         [(h_out["c4f"][r * C4_N:(r + 1) * C4_N], w.c4f[r]) for r in range(C4_W)]),
+            "c4_staged": ([(w.c4s[r], w.h_c4[r * C4_N:(r + 1) * C4_N]) for r in range(C4_W)],
+                          [(h_out["c4s"][r * C4_N:(r + 1) * C4_N], w.c4s[r]) for r in range(C4_W)]),
+        }
+        for W in C5_WS:
+            ins, outs = [], [(h_out[f"c5s{W}"], w.c5_out[W])]
+            for r in range(W):
+                src = w.h_c5[W][r * C5_N:(r + 1) * C5_N]
+                ins += [(w.c5_sum_src[W][r], src), (w.c5_ar[W][r], src)]
+                outs.append((h_out[f"c5a{W}"][r * C5_N:(r + 1) * C5_N], w.c5_ar[W][r]))
+            io[f"c5_w{W}"] = (ins, outs)
+        for n in C2_NS:
+            io[f"c2_{n}"] = ([(w.c2[n], w.h_c2[n])], [(h_out[f"c2{n}"], w.c2_out[n])])
+        return io
+
+    # Two sets of device buffers, alternate steps: the uploads of step k+1
+    # never wait for the read-back of step k (an in-place all-reduce's inputs
+    # are its outputs), so the two directions of the host link overlap. Every
+    # step still uploads all its inputs and reads back all its results.
+    sets = [(wl, rows, io_of(wl))]
+    twin = wl.device_twin()
+    sets.append((twin, twin.rows(), io_of(twin)))
+    io = sets[0][2]
     h2d = sum(d.numel() * 4 for ins, _ in io.values() for d, _ in ins)
     d2h = sum(h.numel() * 4 for _, outs in io.values() for h, _ in outs)
     # one upload and one download stream per row: a row whose buffers are
@@ -924,17 +948,21 @@ def run_gpu(args) -> None:
     s_h2d = {name: torch.cuda.Stream(device=dev) for name, _, _ in rows}
     s_d2h = {name: torch.cuda.Stream(device=dev) for name, _, _ in rows}
     s_cmp = torch.cuda.Stream(device=dev)
-    ev_cmp = {name: None for name, _, _ in rows}
-    ev_d2h = {name: None for name, _, _ in rows}
+    ev_cmp = [{name: None for name, _, _ in rows} for _ in sets]
+    ev_d2h = [{name: None for name, _, _ in rows} for _ in sets]
     # rows that also read a row's uploaded inputs (c3_ptrs folds the C3 rows)
     also_reads = {"c3_stacked": ["c3_ptrs"]}
+    step_no = [0]
 
     def e2e_step():
-        for name, fn, _ in rows:
-            ins, outs = io[name]
+        k = step_no[0] % 2
+        step_no[0] += 1
+        _, set_rows, set_io = sets[k]
+        for name, fn, _ in set_rows:
+            ins, outs = set_io[name]
             up, down = s_h2d[name], s_d2h[name]
             with torch.cuda.stream(up):
-                for ev in [ev_cmp[name], ev_d2h[name]] + [ev_cmp[x] for x in also_reads.get(name, [])]:
+                for ev in [ev_cmp[k][name], ev_d2h[k][name]] + [ev_cmp[k][x] for x in also_reads.get(name, [])]:
                     if ev is not None:
                         up.wait_event(ev)
                 for d, h in ins:
@@ -943,19 +971,20 @@ def run_gpu(args) -> None:
                 landed.record(up)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(landed)
-                if ev_d2h[name] is not None:
-                    s_cmp.wait_event(ev_d2h[name])
+                if ev_d2h[k][name] is not None:
+                    s_cmp.wait_event(ev_d2h[k][name])
                 fn()
-                ev_cmp[name] = torch.cuda.Event()
-                ev_cmp[name].record(s_cmp)
+                ev_cmp[k][name] = torch.cuda.Event()
+                ev_cmp[k][name].record(s_cmp)
             with torch.cuda.stream(down):
-                down.wait_event(ev_cmp[name])
+                down.wait_event(ev_cmp[k][name])
                 for h, d in outs:
                     h.copy_(d, non_blocking=True)
-                ev_d2h[name] = torch.cuda.Event()
-                ev_d2h[name].record(down)
+                ev_d2h[k][name] = torch.cuda.Event()
+                ev_d2h[k][name].record(down)
 
     e2e_step()
+    e2e_step()  # both sets once before timing
     torch.cuda.synchronize()
 
     def e2e_pass() -> float:
@@ -1045,7 +1074,8 @@ def run_gpu(args) -> None:
         "bitwise_sampled": check,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-                "pipelined": "per-row H2D and D2H streams around one compute stream",
+                "pipelined": "per-row H2D and D2H streams around one compute stream; two sets of "
+                             "device buffers, alternate steps",
                 "bitwise_sampled_words_differing": int(e2e_check),
                 "link_bytes_gbs": round(link_gbs, 1),
                 "passes": {"count": E2E_PASSES, "steps_each": e2e_steps,

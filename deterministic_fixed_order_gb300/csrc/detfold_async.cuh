@@ -141,6 +141,37 @@ __device__ __forceinline__ bool named_sync_any(int id, int n, bool pred)
     return r != 0;
 }
 
+#ifndef DETFOLD_BULK_EXCLUSIVE
+#define DETFOLD_BULK_EXCLUSIVE 1  // 1: bulk CTAs reserve shared memory so no SM holds more than planned
+#endif
+
+// Host side. Dynamic shared memory to request per CTA of a grid planned for
+// `per_sm` CTAs on every SM: the kernel's own need, raised (when
+// DETFOLD_BULK_EXCLUSIVE) until a (per_sm + 1)-th CTA no longer fits on an
+// SM. The bulk kernels give every CTA a fixed share of the tiles, so an SM
+// holding an extra CTA would finish last. That happens when programmatic
+// dependent launch places CTAs while the previous kernel still occupies the
+// SMs: measured on GB300, a W=4 all-reduce planned for 2 CTAs per SM in
+// 41 KB each (5 fit) cost a back-to-back step 0.25 ms more than the same
+// kernel run alone.
+static inline cudaError_t exclusive_smem(int dev, size_t need, int per_sm, size_t *out)
+{
+    *out = need;
+    if (!DETFOLD_BULK_EXCLUSIVE || per_sm <= 0) return cudaSuccess;
+    int per_sm_bytes = 0, reserved = 0, optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&per_sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    // (per_sm + 1) * (x + reserved) > per_sm_bytes, rounded up to 128 bytes
+    size_t x = (size_t)(per_sm_bytes / (per_sm + 1) - reserved + 1);
+    x = (x + 127) / 128 * 128;
+    if (x > need && x <= (size_t)optin && (size_t)per_sm * (x + reserved) <= (size_t)per_sm_bytes) *out = x;
+    return cudaSuccess;
+}
+
 // Host side: this translation unit's counter.
 static inline cudaError_t read_unit_timeouts(unsigned long long *count)
 {

@@ -127,6 +127,9 @@
 #ifndef DETFOLD_AR_CTAS_PER_SM
 #define DETFOLD_AR_CTAS_PER_SM 0
 #endif
+#ifndef DETFOLD_FILL_SMS
+#define DETFOLD_FILL_SMS 2  // bandwidth-path grids below this many CTAs per SM use smaller CTAs (0: off)
+#endif
 
 // Cache-hint knobs (compile-time; the defaults are the measured choice).
 #ifndef DETFOLD_LD_L2_PREFETCH

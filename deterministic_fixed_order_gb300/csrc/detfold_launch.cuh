@@ -95,22 +95,55 @@ inline cudaError_t resident_ctas(int threads, int cap_per_sm, int *out)
     return cudaSuccess;
 }
 
+// Streaming multiprocessors of the current device, looked up once per device.
+inline cudaError_t sm_count(int *out)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return cudaSuccess;
+}
+
 // One launch: the small path covers the work exactly with small CTAs; the
 // bandwidth path runs a grid of at most the resident CTAs, each thread
-// striding over U-vector groups. Programmatic dependent launch is used
-// exactly when the parameter block's pdl flag is set.
+// striding over U-vector groups. When the work would give fewer than
+// DETFOLD_FILL_SMS CTAs per SM, the CTA size halves (down to 64 threads), so
+// a medium-sized call spreads over every SM instead of a few large CTAs on
+// some of them. Programmatic dependent launch is used exactly when the
+// parameter block's pdl flag is set.
 template <auto Kernel, typename Params>
 inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool small, int bw_threads,
-                                 int cap_per_sm, cudaStream_t stream)
+                                 int cap_per_sm, cudaStream_t stream, bool fill = true)
 {
-    const int threads = small ? DETFOLD_SMALL_THREADS : bw_threads;
+    int threads = small ? DETFOLD_SMALL_THREADS : bw_threads;
     int64_t blocks = (work + threads - 1) / threads;
     if (!small) {
-        const int64_t per_iter = (int64_t)threads * u;
+        int64_t per_iter = (int64_t)threads * u;
         blocks = (work + per_iter - 1) / per_iter;
         int cap = 0;
-        const cudaError_t e = resident_ctas<Kernel>(threads, cap_per_sm, &cap);
+        cudaError_t e = resident_ctas<Kernel>(threads, cap_per_sm, &cap);
         if (e != cudaSuccess) return e;
+        if (DETFOLD_FILL_SMS > 0 && fill && blocks < cap) {
+            int sms = 0;
+            e = sm_count(&sms);
+            if (e != cudaSuccess) return e;
+            const int64_t want = (int64_t)DETFOLD_FILL_SMS * sms;
+            while (threads > 64 && blocks < want) {
+                threads /= 2;
+                cap *= 2;  // the same resident threads in CTAs of half the size
+                per_iter = (int64_t)threads * u;
+                blocks = (work + per_iter - 1) / per_iter;
+            }
+        }
         if (blocks > cap) blocks = cap;
     }
     if (blocks < 1) blocks = 1;
@@ -171,7 +204,7 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
 }
 
 // Bulk-async (TMA) staged bandwidth path (fold_bulk.cu).
-int bulk_tile_floats(int W);
+int bulk_tile_floats(int W, int mode);  // floats per rank per tile of the bulk path
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream);
 // Large fold or all-reduce over a device-resident pointer table, W <= 8: the
 // bulk-async pipeline when the entries share a 16-byte phase (decided on the
@@ -187,7 +220,7 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
     const bool small = s.len <= DETFOLD_SMALL_LEN;
     const Plan pl = make_plan(s, small ? DETFOLD_SMALL_VEC : DETFOLD_PREFER_VEC);
     if (DETFOLD_USE_BULK && !small && pl.vec >= 4 && s.len >= DETFOLD_BULK_MIN_LEN &&
-        s.len - pl.head >= bulk_tile_floats(W))
+        s.len - pl.head >= bulk_tile_floats(W, MODE))
         return launch_bulk(s, pl.head, stream);
     const FoldParams<W> p = fill_params<W>(s, pl, small);
     constexpr int T = bw_threads<MODE>();
@@ -234,8 +267,9 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         // a warp covers 31 vectors per pass, DETFOLD_REALIGN_U passes per iteration
         const int64_t work = q.nvec > 2 ? (q.nvec - 2 + 30) / 31 * 32 : 32;
         static_assert(DETFOLD_SMALL_THREADS <= DETFOLD_REALIGN_THREADS, "small launches fit the launch bound");
+        // (its CTA size stays: smaller CTAs measured slower for this kernel)
         return launch_kernel<fold_realign_kernel<W, MODE>>(q, work, DETFOLD_REALIGN_U, small,
-                                                           DETFOLD_REALIGN_THREADS, 0, stream);
+                                                           DETFOLD_REALIGN_THREADS, 0, stream, false);
     }
     constexpr int U = u_for<MODE>(W, 0);
     return launch_kernel<fold_scalar_kernel<W, U, MODE>>(p, s.len, U, small, T, C, stream);

@@ -39,7 +39,8 @@ namespace detfold {
 namespace {
 
 // Tile shapes from GB300 sweeps: 8 KB per rank and 3 stages up to W = 4,
-// 4 KB per rank and 2 stages above; four consumer warps.
+// 4 KB per rank and 2 stages above; four consumer warps. The all-reduce has
+// its own knobs (below).
 #ifndef DETFOLD_BULK_T_LO
 #define DETFOLD_BULK_T_LO 2048  // floats per rank per tile, W <= 4
 #endif
@@ -58,13 +59,54 @@ namespace {
 #ifndef DETFOLD_BULK_CTAS_PER_SM
 #define DETFOLD_BULK_CTAS_PER_SM 2  // 0: as many as shared memory allows
 #endif
+// The all-reduce's own shape (it reads and writes W tiles per stage; the sums
+// read W and write one), by default the same as the sums'.
+#ifndef DETFOLD_BULK_AR_T_LO
+#define DETFOLD_BULK_AR_T_LO DETFOLD_BULK_T_LO
+#endif
+#ifndef DETFOLD_BULK_AR_S_LO
+#define DETFOLD_BULK_AR_S_LO DETFOLD_BULK_S_LO
+#endif
+#ifndef DETFOLD_BULK_AR_T_HI
+#define DETFOLD_BULK_AR_T_HI DETFOLD_BULK_T_HI
+#endif
+#ifndef DETFOLD_BULK_AR_S_HI
+#define DETFOLD_BULK_AR_S_HI DETFOLD_BULK_S_HI
+#endif
+#ifndef DETFOLD_BULK_AR_CTAS_PER_SM
+#define DETFOLD_BULK_AR_CTAS_PER_SM DETFOLD_BULK_CTAS_PER_SM
+#endif
+#ifndef DETFOLD_BULK_AR_PER_W
+#define DETFOLD_BULK_AR_PER_W 1  // 1: the all-reduce's shape per W from ArShape; 0: the knobs above
+#endif
+// All-reduce shapes per W (floats per rank per tile, stages, CTAs per SM),
+// from an interleaved A/B sweep on GB300 against the sums' shapes (same
+// bits): W=2 +5%, W=3 +3%, W=4 +2-3% (the 4 x 1e8 call 6.47 -> 6.61 TB/s),
+// W=8 +6%. W=1 and W=5-6 measured faster with the sums' shapes and keep them.
 template <int W>
+struct ArShape {
+    static constexpr int T = W == 1 ? DETFOLD_BULK_T_LO : W <= 3 ? 1024 : W == 4 ? 512
+                           : W <= 6 ? DETFOLD_BULK_T_HI : 256;
+    static constexpr int S = W == 1 ? DETFOLD_BULK_S_LO : W <= 3 ? 2 : W == 4 ? 3
+                           : W <= 6 ? DETFOLD_BULK_S_HI : 3;
+    static constexpr int C = W == 1 ? DETFOLD_BULK_CTAS_PER_SM : W <= 3 ? 3 : 2;
+};
+template <int W, int MODE>
 struct BulkShape {
-    static constexpr int T = W <= 4 ? DETFOLD_BULK_T_LO : DETFOLD_BULK_T_HI;
-    static constexpr int S = W <= 4 ? DETFOLD_BULK_S_LO : DETFOLD_BULK_S_HI;
+    static constexpr bool AR = (MODE == kAllReduce);
+    static constexpr bool PER_W = AR && DETFOLD_BULK_AR_PER_W;
+    static constexpr int T = PER_W ? ArShape<W>::T
+                           : W <= 4 ? (AR ? DETFOLD_BULK_AR_T_LO : DETFOLD_BULK_T_LO)
+                                    : (AR ? DETFOLD_BULK_AR_T_HI : DETFOLD_BULK_T_HI);
+    static constexpr int S = PER_W ? ArShape<W>::S
+                           : W <= 4 ? (AR ? DETFOLD_BULK_AR_S_LO : DETFOLD_BULK_S_LO)
+                                    : (AR ? DETFOLD_BULK_AR_S_HI : DETFOLD_BULK_S_HI);
+    static constexpr int CTAS_PER_SM = PER_W ? ArShape<W>::C
+                                     : (AR ? DETFOLD_BULK_AR_CTAS_PER_SM : DETFOLD_BULK_CTAS_PER_SM);
     static constexpr int NCW = DETFOLD_BULK_NCW;
     static constexpr int THREADS = 32 * (1 + NCW);
     static constexpr size_t SMEM = (size_t)S * (W + 1) * T * 4 + 2 * S * 8;
+    static_assert(T % 4 == 0, "tiles are whole 16-byte vectors (bulk copies move multiples of 16 bytes)");
 };
 
 template <int W>
@@ -87,7 +129,7 @@ struct BulkParams {
 template <int W, int MODE>
 __device__ __forceinline__ void bulk_edges(const BulkParams<W> &p, int tc)
 {
-    constexpr int T = BulkShape<W>::T, NC = 32 * BulkShape<W>::NCW;
+    constexpr int T = BulkShape<W, MODE>::T, NC = 32 * BulkShape<W, MODE>::NCW;
     const int64_t tail0 = p.head + p.ntiles * T;
     const int64_t nv = (p.len - tail0) / 4;
     for (int64_t v = (int64_t)(gridDim.x - 1 - blockIdx.x) * NC + tc; v < nv; v += (int64_t)gridDim.x * NC) {
@@ -131,7 +173,7 @@ __device__ __forceinline__ void bulk_edges(const BulkParams<W> &p, int tc)
 
 // The dynamic shared memory of a bulk CTA: S stages of W input tiles and one
 // result tile, then the full and empty mbarriers of every stage.
-template <int W>
+template <int W, int MODE>
 struct BulkSmem {
     float *in;        // [S][W][T]
     float *res;       // [S][T]
@@ -139,11 +181,11 @@ struct BulkSmem {
     uint64_t *empty;  // [S]
 };
 
-template <int W>
-__device__ __forceinline__ BulkSmem<W> bulk_smem_init(unsigned char *smem)
+template <int W, int MODE>
+__device__ __forceinline__ BulkSmem<W, MODE> bulk_smem_init(unsigned char *smem)
 {
-    using Sh = BulkShape<W>;
-    BulkSmem<W> m;
+    using Sh = BulkShape<W, MODE>;
+    BulkSmem<W, MODE> m;
     m.in = (float *)smem;
     m.res = m.in + (size_t)Sh::S * W * Sh::T;
     m.full = (uint64_t *)(m.res + (size_t)Sh::S * Sh::T);
@@ -162,9 +204,9 @@ __device__ __forceinline__ BulkSmem<W> bulk_smem_init(unsigned char *smem)
 // the producer lane streams the CTA's tiles, the consumer warps fold them
 // and store the results, and first fold the call's edges.
 template <int W, int MODE>
-__device__ __forceinline__ void bulk_run(const BulkParams<W> &p, const BulkSmem<W> &m)
+__device__ __forceinline__ void bulk_run(const BulkParams<W> &p, const BulkSmem<W, MODE> &m)
 {
-    using Sh = BulkShape<W>;
+    using Sh = BulkShape<W, MODE>;
     constexpr int T = Sh::T, S = Sh::S, NC = 32 * Sh::NCW;
     float *in = m.in, *res = m.res;
     uint64_t *full = m.full, *empty = m.empty;
@@ -237,10 +279,10 @@ __device__ __forceinline__ void bulk_run(const BulkParams<W> &p, const BulkSmem<
 }
 
 template <int W, int MODE>
-__global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_kernel(const __grid_constant__ BulkParams<W> p)
+__global__ void __launch_bounds__(BulkShape<W, MODE>::THREADS) fold_bulk_kernel(const __grid_constant__ BulkParams<W> p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    const BulkSmem<W> m = bulk_smem_init<W>(smem);
+    const BulkSmem<W, MODE> m = bulk_smem_init<W, MODE>(smem);
     pdl_enter(p.pdl);
     __syncthreads();
     bulk_run<W, MODE>(p, m);
@@ -264,13 +306,13 @@ struct BulkTableParams {
 // output) shares one 16-byte phase, the CTA runs the same bulk pipeline as
 // fold_bulk_kernel; otherwise the grid folds with coalesced scalar accesses.
 template <int W, int MODE>
-__global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_table_kernel(const __grid_constant__ BulkTableParams tp)
+__global__ void __launch_bounds__(BulkShape<W, MODE>::THREADS) fold_bulk_table_kernel(const __grid_constant__ BulkTableParams tp)
 {
-    constexpr int T = BulkShape<W>::T;
+    constexpr int T = BulkShape<W, MODE>::T;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ BulkParams<W> sp;
     __shared__ int s_code, s_bulk;
-    const BulkSmem<W> m = bulk_smem_init<W>(smem);
+    const BulkSmem<W, MODE> m = bulk_smem_init<W, MODE>(smem);
     pdl_enter(tp.pdl);
     if (threadIdx.x == 0) {
         int code = DETFOLD_OK;
@@ -321,39 +363,48 @@ __global__ void __launch_bounds__(BulkShape<W>::THREADS) fold_bulk_table_kernel(
     }
 }
 
-// Shared-memory opt-in and resident CTAs, once per kernel and device.
-template <auto Kernel, int W>
-cudaError_t bulk_grid_of(int *grid)
+// Shared-memory opt-in, resident CTAs and the per-CTA shared-memory request
+// (exclusive_smem), once per kernel and device.
+template <auto Kernel, int W, int MODE>
+cudaError_t bulk_grid_of(int *grid, int *smem_bytes)
 {
-    static std::atomic<int> cache[64];
+    static std::atomic<int> cache[64], cache_smem[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int v = cache[dev].load(std::memory_order_relaxed);
+    int v = cache[dev].load(std::memory_order_acquire);
     if (v <= 0) {
-        using Sh = BulkShape<W>;
-        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)Sh::SMEM);
+        using Sh = BulkShape<W, MODE>;
+        e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM);
         if (e != cudaSuccess) return e;
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kernel, Sh::THREADS,
-                                                          Sh::SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, Kernel, Sh::THREADS, Sh::SMEM);
         if (e != cudaSuccess) return e;
-        if (DETFOLD_BULK_CTAS_PER_SM > 0 && per_sm > DETFOLD_BULK_CTAS_PER_SM) per_sm = DETFOLD_BULK_CTAS_PER_SM;
-        v = sms * (per_sm > 0 ? per_sm : 1);
-        cache[dev].store(v, std::memory_order_relaxed);
+        if (Sh::CTAS_PER_SM > 0 && per_sm > Sh::CTAS_PER_SM) per_sm = Sh::CTAS_PER_SM;
+        if (per_sm < 1) per_sm = 1;
+        size_t smem = Sh::SMEM;
+        e = exclusive_smem(dev, Sh::SMEM, per_sm, &smem);
+        if (e != cudaSuccess) return e;
+        if (smem != Sh::SMEM) {
+            e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        cache_smem[dev].store((int)smem, std::memory_order_relaxed);
+        v = sms * per_sm;
+        cache[dev].store(v, std::memory_order_release);
     }
     *grid = v;
+    *smem_bytes = cache_smem[dev].load(std::memory_order_relaxed);
     return cudaSuccess;
 }
 
 template <int W, int MODE>
 cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t stream)
 {
-    using Sh = BulkShape<W>;
+    using Sh = BulkShape<W, MODE>;
     BulkParams<W> p = {};
     for (int r = 0; r < W; ++r) p.a[r] = const_cast<float *>(s.src[r]);
     p.out = s.out;
@@ -363,15 +414,15 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
     p.scale = s.scale;
     p.do_scale = s.do_scale;
     p.pdl = DETFOLD_PDL_ALL ? 1 : 0;
-    int cap = 0;
-    cudaError_t e = bulk_grid_of<fold_bulk_kernel<W, MODE>, W>(&cap);
+    int cap = 0, smem = 0;
+    cudaError_t e = bulk_grid_of<fold_bulk_kernel<W, MODE>, W, MODE>(&cap, &smem);
     if (e != cudaSuccess) return e;
     int64_t grid = p.ntiles < cap ? p.ntiles : cap;
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(Sh::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (p.pdl) {
@@ -386,9 +437,9 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
 template <int W, int MODE>
 cudaError_t launch_bulk_table_fixed(const BulkTableParams &tp, cudaStream_t stream)
 {
-    using Sh = BulkShape<W>;
-    int cap = 0;
-    cudaError_t e = bulk_grid_of<fold_bulk_table_kernel<W, MODE>, W>(&cap);
+    using Sh = BulkShape<W, MODE>;
+    int cap = 0, smem = 0;
+    cudaError_t e = bulk_grid_of<fold_bulk_table_kernel<W, MODE>, W, MODE>(&cap, &smem);
     if (e != cudaSuccess) return e;
     int64_t grid = tp.len / Sh::T;  // about one CTA per tile, at most the resident CTAs
     if (grid > cap) grid = cap;
@@ -396,7 +447,7 @@ cudaError_t launch_bulk_table_fixed(const BulkTableParams &tp, cudaStream_t stre
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(Sh::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (tp.pdl) {
@@ -442,7 +493,25 @@ cudaError_t launch_bulk_mode(const LaunchSpec &s, int64_t head, cudaStream_t str
 
 cudaError_t read_pipeline_timeouts_bulk(unsigned long long *count) { return read_unit_timeouts(count); }
 
-int bulk_tile_floats(int W) { return W <= 4 ? BulkShape<4>::T : BulkShape<8>::T; }
+template <int MODE>
+int tile_floats_of(int W)
+{
+    switch (W) {
+    case 1: return BulkShape<1, MODE>::T;
+    case 2: return BulkShape<2, MODE>::T;
+    case 3: return BulkShape<3, MODE>::T;
+    case 4: return BulkShape<4, MODE>::T;
+    case 5: return BulkShape<5, MODE>::T;
+    case 6: return BulkShape<6, MODE>::T;
+    case 7: return BulkShape<7, MODE>::T;
+    default: return BulkShape<8, MODE>::T;
+    }
+}
+
+int bulk_tile_floats(int W, int mode)
+{
+    return mode == kAllReduce ? tile_floats_of<kAllReduce>(W) : tile_floats_of<kSumCoherent>(W);
+}
 
 cudaError_t launch_bulk_table(const float *const *d_table, float *out, int *d_status, int W, int64_t len,
                               float scale, int do_scale, int mode, cudaStream_t stream)

@@ -137,12 +137,14 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
     p.len = len;
     p.head = head;
     p.ntiles = (len - head) / Sh::T;
-    static std::atomic<int> cache[64];
+    // resident CTAs (at most 4 per SM) and the per-CTA shared-memory request
+    // that keeps every SM at that count (exclusive_smem), once per device
+    static std::atomic<int> cache[64], cache_smem[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int cap = cache[dev].load(std::memory_order_relaxed);
+    int cap = cache[dev].load(std::memory_order_acquire);
     if (cap <= 0) {
         e = cudaFuncSetAttribute(move_bulk_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM);
         if (e != cudaSuccess) return e;
@@ -152,15 +154,24 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, move_bulk_kernel<G>, 64, Sh::SMEM);
         if (e != cudaSuccess) return e;
         if (per_sm > 4) per_sm = 4;
-        cap = sms * (per_sm > 0 ? per_sm : 1);
-        cache[dev].store(cap, std::memory_order_relaxed);
+        if (per_sm < 1) per_sm = 1;
+        size_t smem = Sh::SMEM;
+        e = exclusive_smem(dev, Sh::SMEM, per_sm, &smem);
+        if (e != cudaSuccess) return e;
+        if (smem != Sh::SMEM) {
+            e = cudaFuncSetAttribute(move_bulk_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        cache_smem[dev].store((int)smem, std::memory_order_relaxed);
+        cap = sms * per_sm;
+        cache[dev].store(cap, std::memory_order_release);
     }
     int64_t grid = p.ntiles < cap ? p.ntiles : cap;
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(64, 1, 1);
-    cfg.dynamicSmemBytes = Sh::SMEM;
+    cfg.dynamicSmemBytes = (size_t)cache_smem[dev].load(std::memory_order_relaxed);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (p.pdl) {

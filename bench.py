@@ -64,11 +64,11 @@ E2E_PASSES = 5  # end-to-end passes; `e2e.value` is their median
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147588352 + 259558912,
-                                  "kernel_hash": "2abd361dee919241"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147520512 + 258758912,
+                                  "kernel_hash": "c745789a938f71a2"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600031232 + 1538103296,
-                                         "kernel_hash": "2abd361dee919241"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600032000 + 1538616320,
+                                         "kernel_hash": "c745789a938f71a2"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",
@@ -633,6 +633,34 @@ def host_link_gbs(torch, dev, reps: int = 5) -> dict:
     return res
 
 
+class LinkSample:
+    """A short both-ways sample of the host link (256 MiB each way on two
+    streams, median of 3), taken right after each end-to-end pass, so that a
+    slow pass can be set against the link's rate at that moment."""
+
+    def __init__(self, torch, dev, n: int = 1 << 26):
+        self.torch = torch
+        self.h_in = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        self.h_out = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        self.d_a = torch.empty(n, dtype=torch.float32, device=dev)
+        self.d_b = torch.empty(n, dtype=torch.float32, device=dev)
+        self.up, self.down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        self.nbytes = 2 * n * 4
+
+    def __call__(self, reps: int = 3) -> float:
+        torch, ts = self.torch, []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(self.up):
+                self.d_a.copy_(self.h_in, non_blocking=True)
+            with torch.cuda.stream(self.down):
+                self.h_out.copy_(self.d_b, non_blocking=True)
+            torch.cuda.synchronize()
+            ts.append(self.nbytes / (time.perf_counter() - t0) / 1e9)
+        return statistics.median(ts)
+
+
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context only)
 
 
@@ -983,8 +1011,8 @@ def run_gpu(args) -> None:
                 ev_d2h[k][name] = torch.cuda.Event()
                 ev_d2h[k][name].record(down)
 
-    e2e_step()
-    e2e_step()  # both sets once before timing
+    for _ in range(4):  # both sets twice before timing: first copies from fresh pinned buffers run slow
+        e2e_step()
     torch.cuda.synchronize()
 
     def e2e_pass() -> float:
@@ -1011,7 +1039,12 @@ def run_gpu(args) -> None:
     # the end-to-end figure is link-bound, so its spread is read against the
     # link's own rate at the time
     link_before = host_link_gbs(torch, dev)
-    pass_ms = [e2e_pass() for _ in range(E2E_PASSES)]
+    sample = LinkSample(torch, dev)
+    pass_ms, pass_link = [], []
+    for _ in range(E2E_PASSES):
+        pass_ms.append(e2e_pass())
+        pass_link.append(sample())
+    del sample
     link = host_link_gbs(torch, dev)
     e2e_ms = statistics.median(pass_ms)
     e2e_value = whole_job_gbs(world, step_bytes, e2e_ms)
@@ -1080,7 +1113,11 @@ def run_gpu(args) -> None:
                 "link_bytes_gbs": round(link_gbs, 1),
                 "passes": {"count": E2E_PASSES, "steps_each": e2e_steps,
                            "gbs_min": round(pass_gbs[0], 1), "gbs_median": round(e2e_value, 1),
-                           "gbs_max": round(pass_gbs[-1], 1)},
+                           "gbs_max": round(pass_gbs[-1], 1),
+                           "each": [{"gbs": round(whole_job_gbs(world, step_bytes, m), 1),
+                                     "link_step_gbs": round((h2d + d2h) / (m * 1e-3) / 1e9, 1),
+                                     "link_sample_both_gbs": round(l, 1)}
+                                    for m, l in zip(pass_ms, pass_link)]},
                 "link_this_run": {k: round(v, 1) for k, v in link.items()},
                 "link_before_passes": {k: round(v, 1) for k, v in link_before.items()},
                 "link_utilisation_of_both_ways": round(link_gbs / link["both_gbs"], 3)},

@@ -38,14 +38,14 @@ namespace detfold {
 
 namespace {
 
-// Tile shapes from GB300 sweeps: 8 KB per rank and 3 stages up to W = 4,
+// Tile shapes from GB300 sweeps: 4 KB per rank and 4 stages up to W = 4,
 // 4 KB per rank and 2 stages above; four consumer warps. The all-reduce has
-// its own knobs (below).
+// its own shapes (below).
 #ifndef DETFOLD_BULK_T_LO
-#define DETFOLD_BULK_T_LO 2048  // floats per rank per tile, W <= 4
+#define DETFOLD_BULK_T_LO 1024  // floats per rank per tile, W <= 4
 #endif
 #ifndef DETFOLD_BULK_S_LO
-#define DETFOLD_BULK_S_LO 3     // stages, W <= 4
+#define DETFOLD_BULK_S_LO 4     // stages, W <= 4
 #endif
 #ifndef DETFOLD_BULK_T_HI
 #define DETFOLD_BULK_T_HI 1024  // floats per rank per tile, W > 4
@@ -85,11 +85,9 @@ namespace {
 // W=8 +6%. W=1 and W=5-6 measured faster with the sums' shapes and keep them.
 template <int W>
 struct ArShape {
-    static constexpr int T = W == 1 ? DETFOLD_BULK_T_LO : W <= 3 ? 1024 : W == 4 ? 512
-                           : W <= 6 ? DETFOLD_BULK_T_HI : 256;
-    static constexpr int S = W == 1 ? DETFOLD_BULK_S_LO : W <= 3 ? 2 : W == 4 ? 3
-                           : W <= 6 ? DETFOLD_BULK_S_HI : 3;
-    static constexpr int C = W == 1 ? DETFOLD_BULK_CTAS_PER_SM : W <= 3 ? 3 : 2;
+    static constexpr int T = W == 1 ? 2048 : W <= 3 ? 1024 : W == 4 ? 512 : W <= 6 ? 1024 : 256;
+    static constexpr int S = W == 1 ? 3 : W <= 3 ? 2 : W == 4 ? 3 : W <= 6 ? 2 : 3;
+    static constexpr int C = W <= 3 && W > 1 ? 3 : 2;
 };
 template <int W, int MODE>
 struct BulkShape {

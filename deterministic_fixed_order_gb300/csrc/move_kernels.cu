@@ -32,11 +32,24 @@ namespace {
 // several destinations (a distribute phase, a broadcast) is read from DRAM
 // once. A stage is released only after the stores reading it have finished
 // reading (wait_group.read). Waits are bounded (detfold_async.cuh).
+#ifndef DETFOLD_MOVE_T
+#define DETFOLD_MOVE_T 2048  // floats per source per tile (8 KB)
+#endif
+#ifndef DETFOLD_MOVE_S_LO
+#define DETFOLD_MOVE_S_LO 4  // stages, up to 4 distinct sources
+#endif
+#ifndef DETFOLD_MOVE_S_HI
+#define DETFOLD_MOVE_S_HI 2  // stages, more sources
+#endif
+#ifndef DETFOLD_MOVE_CTAS_PER_SM
+#define DETFOLD_MOVE_CTAS_PER_SM 4
+#endif
 template <int G>
 struct MoveShape {
-    static constexpr int T = 2048;              // floats per source per tile (8 KB)
-    static constexpr int S = G <= 4 ? 4 : 2;    // stages
+    static constexpr int T = DETFOLD_MOVE_T;
+    static constexpr int S = G <= 4 ? DETFOLD_MOVE_S_LO : DETFOLD_MOVE_S_HI;
     static constexpr size_t SMEM = (size_t)S * G * T * 4 + 2 * S * 8;
+    static_assert(T % 4 == 0, "tiles are whole 16-byte vectors");
 };
 
 template <int G>
@@ -137,7 +150,7 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
     p.len = len;
     p.head = head;
     p.ntiles = (len - head) / Sh::T;
-    // resident CTAs (at most 4 per SM) and the per-CTA shared-memory request
+    // resident CTAs (at most DETFOLD_MOVE_CTAS_PER_SM) and the per-CTA shared-memory request
     // that keeps every SM at that count (exclusive_smem), once per device
     static std::atomic<int> cache[64], cache_smem[64];
     int dev = 0;
@@ -153,7 +166,7 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
         if (e != cudaSuccess) return e;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, move_bulk_kernel<G>, 64, Sh::SMEM);
         if (e != cudaSuccess) return e;
-        if (per_sm > 4) per_sm = 4;
+        if (per_sm > DETFOLD_MOVE_CTAS_PER_SM) per_sm = DETFOLD_MOVE_CTAS_PER_SM;
         if (per_sm < 1) per_sm = 1;
         size_t smem = Sh::SMEM;
         e = exclusive_smem(dev, Sh::SMEM, per_sm, &smem);

@@ -982,7 +982,7 @@ def run_gpu(args) -> None:
     also_reads = {"c3_stacked": ["c3_ptrs"]}
     step_no = [0]
 
-    def e2e_step():
+    def e2e_step(compute: bool = True):
         k = step_no[0] % 2
         step_no[0] += 1
         _, set_rows, set_io = sets[k]
@@ -1001,7 +1001,8 @@ def run_gpu(args) -> None:
                 s_cmp.wait_event(landed)
                 if ev_d2h[k][name] is not None:
                     s_cmp.wait_event(ev_d2h[k][name])
-                fn()
+                if compute:
+                    fn()
                 ev_cmp[k][name] = torch.cuda.Event()
                 ev_cmp[k][name].record(s_cmp)
             with torch.cuda.stream(down):
@@ -1038,13 +1039,30 @@ def run_gpu(args) -> None:
     # the host link is measured before and after the passes, in this run:
     # the end-to-end figure is link-bound, so its spread is read against the
     # link's own rate at the time
+    def copies_only_ms(steps: int = 3) -> tuple[float, float]:
+        """ms of single steps of the same uploads and read-backs with no
+        kernels (fastest, slowest of `steps`): the link's own rate for this
+        step's transfers at this moment."""
+        ts = []
+        for _ in range(steps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step(compute=False)
+            torch.cuda.synchronize()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        return min(ts), max(ts)
+
     link_before = host_link_gbs(torch, dev)
     sample = LinkSample(torch, dev)
-    pass_ms, pass_link = [], []
+    pass_ms, pass_link, pass_copies = [], [], []
     for _ in range(E2E_PASSES):
         pass_ms.append(e2e_pass())
+        pass_copies.append(copies_only_ms())
         pass_link.append(sample())
     del sample
+    e2e_step()  # leave the last results of a real step in the host buffers
+    e2e_step()
+    torch.cuda.synchronize()
     link = host_link_gbs(torch, dev)
     e2e_ms = statistics.median(pass_ms)
     e2e_value = whole_job_gbs(world, step_bytes, e2e_ms)
@@ -1115,9 +1133,12 @@ def run_gpu(args) -> None:
                            "gbs_min": round(pass_gbs[0], 1), "gbs_median": round(e2e_value, 1),
                            "gbs_max": round(pass_gbs[-1], 1),
                            "each": [{"gbs": round(whole_job_gbs(world, step_bytes, m), 1),
+                                     "ms_per_step": round(m, 2),
+                                     "copies_only_ms_min_max": [round(c[0], 2), round(c[1], 2)],
+                                     "of_fastest_copies_only": round(c[0] / m, 3),
                                      "link_step_gbs": round((h2d + d2h) / (m * 1e-3) / 1e9, 1),
                                      "link_sample_both_gbs": round(l, 1)}
-                                    for m, l in zip(pass_ms, pass_link)]},
+                                    for m, c, l in zip(pass_ms, pass_copies, pass_link)]},
                 "link_this_run": {k: round(v, 1) for k, v in link.items()},
                 "link_before_passes": {k: round(v, 1) for k, v in link_before.items()},
                 "link_utilisation_of_both_ways": round(link_gbs / link["both_gbs"], 3)},

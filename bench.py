@@ -453,9 +453,13 @@ def graph_us_per_call(torch, df, wl, rounds: int = 5, reps: int = 5) -> dict:
     return res
 
 
-def next_rows(torch, df, wl, reps: int = 10) -> dict:
-    """Rows beyond the step: pure-movement broadcast and all-gather, and the
-    fold over a device-resident pointer table, in algorithmic GB/s."""
+def next_rows(torch, df, wl, reps: int = 10, calls: int = 5) -> dict:
+    """Rows beyond the step: pure-movement broadcast and all-gather, the
+    all-reduce at mixed phases, the realigned stack and the fold over a
+    device-resident pointer table, in algorithmic GB/s. Every operand is
+    larger than L2, and each row is timed as `calls` back-to-back calls
+    between two events (ms per call, median of `reps`), so a figure is the
+    row's streaming rate, not one call's launch and ramp."""
     def t(fn):
         for _ in range(3):
             fn()
@@ -465,10 +469,11 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            for _ in range(calls):
+                fn()
             b.record()
             b.synchronize()
-            ms.append(a.elapsed_time(b))
+            ms.append(a.elapsed_time(b) / calls)
         return statistics.median(ms)
     out = {}
     # broadcast: C3 row 0 to the other seven rows' worth of space (reads 1, writes 7)
@@ -579,12 +584,12 @@ def next_rows(torch, df, wl, reps: int = 10) -> dict:
         for a in arenas:
             a.normal_()
         m = df.detfold_mean_scale(W)
-        ms = t(lambda: [df.detfold_loopback_allreduce(arenas, W, n, m) for _ in range(10)]) / 10
+        ms = t(lambda: df.detfold_loopback_allreduce(arenas, W, n, m))
         out[f"allreduce_mixed_phase_W{W}_2^24"] = {
             "ms": round(ms, 4), "gbs": round(2 * W * n * 4 / (ms * 1e-3) / 1e9, 1),
-            "phases_bytes": [4 * phase(r) for r in range(W)],
-            "timing": "10 back-to-back calls per event pair (arenas larger than L2)"}
+            "phases_bytes": [4 * phase(r) for r in range(W)]}
     del bufs
+    out["timing"] = f"the large rows: {calls} back-to-back calls per event pair, median of {reps}"
     return out
 
 

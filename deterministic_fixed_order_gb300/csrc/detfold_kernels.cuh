@@ -21,7 +21,8 @@
 //   fold_scalar_kernel    the all-reduce at mismatched phases when
 //                         DETFOLD_AR_REALIGN is 0;
 //   fold_vec/scalar_generic_kernel   8 < W <= 256.
-// Large aligned calls take the bulk-async (TMA) kernels of fold_bulk.cu;
+// Large aligned calls, and large all-reduces whose arenas sit at different
+// 16-byte phases, take the bulk-async (TMA) kernels of fold_bulk.cu;
 // device-resident pointer tables take fold_table.cu.
 //
 // Modes:
@@ -87,6 +88,9 @@
 #endif
 #ifndef DETFOLD_USE_BULK
 #define DETFOLD_USE_BULK 1  // bulk-async (TMA) staged path for large aligned calls
+#endif
+#ifndef DETFOLD_BULK_MIXED
+#define DETFOLD_BULK_MIXED 1  // large all-reduce at mixed 16-byte phases: the bulk-async pipeline
 #endif
 #ifndef DETFOLD_AR_REALIGN
 #define DETFOLD_AR_REALIGN 1  // all-reduce at mismatched phases: realigned vectors (0: scalar kernel)

@@ -1,9 +1,10 @@
 // Host-side launch plumbing shared by the mode translation units: phase
 // planning (vector width, head, body, tail), grid sizing, the typed launch
 // of one kernel instantiation, and the dispatch order of a fold call:
-// bulk-async path (large, aligned, W <= 8) -> small-payload kernel (small,
-// common phase) -> vector kernel (common phase) -> realigned vectors
-// (mismatched phases).
+// bulk-async path (large, one 16-byte phase, W <= 8) -> small-payload kernel
+// (small, common phase) -> vector kernel (common phase) -> the bulk-async
+// all-reduce with per-arena offsets (large, mixed 16-byte phases) ->
+// realigned vectors (mismatched phases).
 #pragma once
 
 #include <atomic>
@@ -206,6 +207,8 @@ inline FoldParams<NT> fill_params(const LaunchSpec &s, const Plan &pl, bool smal
 // Bulk-async (TMA) staged bandwidth path (fold_bulk.cu).
 int bulk_tile_floats(int W, int mode);  // floats per rank per tile of the bulk path
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream);
+// The bulk-async all-reduce for arenas at different 16-byte phases, W <= 8.
+cudaError_t launch_bulk_mixed(const LaunchSpec &s, cudaStream_t stream);
 // Large fold or all-reduce over a device-resident pointer table, W <= 8: the
 // bulk-async pipeline when the entries share a 16-byte phase (decided on the
 // device), else a scalar fold; same status word as the other table kernels.
@@ -246,6 +249,12 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         constexpr int U = u_for<MODE>(W, 4);
         constexpr int VT = vec_threads<W, 4, U, MODE>();
         return launch_kernel<fold_vec_kernel<W, 4, U, MODE>>(p, pl.nvec, U, small, VT, C * (T / VT), stream);
+    }
+    if constexpr (MODE == kAllReduce) {
+        // no common 16-byte phase, large: the bulk-async pipeline with
+        // per-arena offsets (fold_bulk.cu)
+        if (DETFOLD_USE_BULK && DETFOLD_BULK_MIXED && !small && pl.vec == 0 && s.len >= DETFOLD_BULK_MIN_LEN)
+            return launch_bulk_mixed(s, stream);
     }
     if (MODE != kAllReduce || DETFOLD_AR_REALIGN) {
         // no common phase: realign every operand onto one 32-byte grid, the

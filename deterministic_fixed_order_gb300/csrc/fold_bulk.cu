@@ -1,5 +1,6 @@
 // Bandwidth path with bulk-async (TMA) staging: the fold and the fused
-// all-reduce for large aligned calls.
+// all-reduce for large aligned calls, and the all-reduce for large calls
+// whose arenas sit at different 16-byte phases (fold_bulk_mixed_kernel).
 //
 // Per CTA, one producer lane streams tiles of every rank's operand into a
 // ring of shared-memory stages with cp.async.bulk (global -> shared,
@@ -361,9 +362,173 @@ __global__ void __launch_bounds__(BulkShape<W, MODE>::THREADS) fold_bulk_table_k
     }
 }
 
+// ---------------------------------------------------------------- arenas at different 16-byte phases
+
+// The all-reduce when the arenas do not share a 16-byte phase. Tiles follow
+// arena 0's 16-byte grid, starting `base` (4..7) elements in. Arena r's
+// elements of a tile begin p_r (0..3) elements past a 16-byte boundary, so
+// its tile is loaded from that boundary, T + 4 floats long (a whole number
+// of 16-byte units), and read at offset p_r in shared memory. The folded
+// tile is written to shared memory once unshifted and once per shift
+// q = (4 - p_r) mod 4 that some arena needs; arena r's 16-byte-aligned
+// interior (T - 4 floats when p_r != 0) then leaves with one bulk store from
+// the copy shifted by q_r, and its two partial 16-byte units (q_r and p_r
+// elements) with scalar stores. Every element is written once, by the CTA
+// that folded it; the elements a tile's loads cover beyond its own range
+// are never used, so the update in place needs no ordering between CTAs.
+// The call's head [0, base) and tail after the last whole tile are scalar.
+template <int W>
+struct MixedParams {
+    float *a[W];   // the arenas, read and written
+    int p[W];      // element phase (0..3) of each arena's tile starts
+    int qmask;     // bit q: some arena stores from the copy shifted by q
+    int64_t len, base, ntiles;
+    float scale;
+    int do_scale;
+    int pdl;
+};
+
+// Shapes from a GB300 sweep (2^24 per arena, identical bits): up to W = 5,
+// 4 KB tiles in 2 stages at up to 4 CTAs per SM (as many as shared memory
+// holds: 3 from W = 3 on); above, 8 KB tiles in 2 stages at one CTA per SM.
+// The limit is the bytes each SM keeps in flight (2 CTAs of 4 KB tiles at
+// W = 3 ran 18% slower). DETFOLD_MIXED_T/_S/_C, when defined, override
+// every W.
+#ifdef DETFOLD_MIXED_T
+#define DETFOLD_MIXED_T_OF(W) DETFOLD_MIXED_T
+#else
+#define DETFOLD_MIXED_T_OF(W) ((W) <= 5 ? 1024 : 2048)
+#endif
+#ifdef DETFOLD_MIXED_S
+#define DETFOLD_MIXED_S_OF(W) DETFOLD_MIXED_S
+#else
+#define DETFOLD_MIXED_S_OF(W) 2
+#endif
+#ifdef DETFOLD_MIXED_C
+#define DETFOLD_MIXED_C_OF(W) DETFOLD_MIXED_C
+#else
+#define DETFOLD_MIXED_C_OF(W) ((W) <= 5 ? 4 : 1)
+#endif
+template <int W>
+struct MixedShape {
+    static constexpr int T = DETFOLD_MIXED_T_OF(W), S = DETFOLD_MIXED_S_OF(W), CTAS_PER_SM = DETFOLD_MIXED_C_OF(W);
+    static constexpr int TL = T + 4;  // floats loaded per arena and tile
+    static constexpr int NCW = DETFOLD_BULK_NCW;
+    static constexpr int THREADS = 32 * (1 + NCW);
+    static constexpr size_t SMEM = (size_t)S * W * TL * 4 + (size_t)S * 4 * T * 4 + 2 * S * 8;
+    static_assert(T % 4 == 0 && T >= 8, "tiles of whole 16-byte units, with an interior");
+    static_assert(8 * W <= 32 * NCW, "one consumer thread per partial element");
+};
+
+template <int W>
+__global__ void __launch_bounds__(MixedShape<W>::THREADS) fold_bulk_mixed_kernel(const __grid_constant__ MixedParams<W> p)
+{
+    using Sh = MixedShape<W>;
+    constexpr int T = Sh::T, S = Sh::S, TL = Sh::TL, NC = 32 * Sh::NCW;
+    extern __shared__ __align__(128) unsigned char smem[];
+    float *in = (float *)smem;                          // [S][W][TL]
+    float *res = in + (size_t)S * W * TL;               // [S][4][T]: copy q is shifted by q
+    uint64_t *full = (uint64_t *)(res + (size_t)S * 4 * T);
+    uint64_t *empty = full + S;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_enter(p.pdl);
+    __syncthreads();
+
+    if (threadIdx.x < 32) {  // producer warp: one lane issues the loads
+        if (threadIdx.x == 0) {
+            long long k = 0;
+            for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
+                const int s = (int)(k % S);
+                if (k >= S && !mbar_wait(&empty[s], (uint32_t)(((k / S) - 1) & 1))) break;
+                mbar_arrive_expect(&full[s], W * TL * 4);
+#pragma unroll
+                for (int r = 0; r < W; ++r)
+                    bulk_load(in + ((size_t)s * W + r) * TL, p.a[r] + p.base + t * T - p.p[r], TL * 4, &full[s]);
+            }
+            for (long long j = (k > S ? k - S : 0); j < k; ++j)  // own copies landed
+                if (!mbar_wait(&full[j % S], (uint32_t)((j / S) & 1))) break;
+        }
+        return;
+    }
+
+    const int tc = threadIdx.x - 32;
+    {   // the call's head and tail, scalar, while the first loads are in flight
+        const int64_t tail0 = p.base + p.ntiles * T;
+        const int64_t nhead = p.ntiles ? p.base : p.len, ntail = p.ntiles ? p.len - tail0 : 0;
+        for (int64_t idx = (int64_t)blockIdx.x * NC + tc; idx < nhead + ntail; idx += (int64_t)gridDim.x * NC) {
+            const int64_t e = idx < nhead ? idx : tail0 + (idx - nhead);
+            float acc = ld1<false>(p.a[0] + e);
+#pragma unroll
+            for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, ld1<false>(p.a[r] + e));
+            if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+#pragma unroll
+            for (int r = 0; r < W; ++r) st1(p.a[r] + e, acc);
+        }
+    }
+    long long k = 0;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++k) {
+        const int s = (int)(k % S);
+        // each consumer waits (bounded) for the stage; the vote gives all
+        // consumers one verdict (as in bulk_run)
+        const bool landed = mbar_wait(&full[s], (uint32_t)((k / S) & 1));
+        if (tc == 0 && landed) bulk_wait_read<S - 1>();  // the stores of tile k-S have read res[s]
+        if (named_sync_any(1, NC, !landed)) break;
+        const float *src = in + (size_t)s * W * TL;
+        float *rq = res + (size_t)s * 4 * T;
+        for (int j = tc * 4; j < T; j += NC * 4) {
+            float acc[4];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) acc[kk] = src[p.p[0] + j + kk];
+#pragma unroll
+            for (int r = 1; r < W; ++r)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) acc[kk] = __fadd_rn(acc[kk], src[(size_t)r * TL + p.p[r] + j + kk]);
+            if (p.do_scale) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) acc[kk] = __fmul_rn(acc[kk], p.scale);
+            }
+            *(float4 *)(rq + j) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+            for (int q = 1; q < 4; ++q) {
+                if (p.qmask & (1 << q)) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int e = j + kk;  // copy q holds elements q .. T-5+q
+                        if (e >= q && e < T - 4 + q) rq[q * T + e - q] = acc[kk];
+                    }
+                }
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk store
+        named_sync(1, NC);
+        const int64_t ts = p.base + t * T;
+        if (tc < 8 * W) {  // the partial 16-byte units at the tile's two ends
+            const int r = tc >> 3, kk = tc & 7, pr = p.p[r], qr = (4 - pr) & 3;
+            const int e = kk < 4 ? (kk < qr ? kk : -1) : (kk - 4 < pr ? T - pr + (kk - 4) : -1);
+            if (e >= 0) st1(p.a[r] + ts + e, rq[e]);
+        }
+        if (tc == 0) {
+            mbar_arrive(&empty[s]);  // the input stage may be refilled
+#pragma unroll
+            for (int r = 0; r < W; ++r) {
+                const int qr = (4 - p.p[r]) & 3;
+                bulk_store(p.a[r] + ts + qr, rq + (size_t)qr * T, (qr ? T - 4 : T) * 4);
+            }
+            bulk_commit();
+        }
+    }
+    if (tc == 0) bulk_wait_all();
+}
+
 // Shared-memory opt-in, resident CTAs and the per-CTA shared-memory request
 // (exclusive_smem), once per kernel and device.
-template <auto Kernel, int W, int MODE>
+template <auto Kernel, typename Sh>
 cudaError_t bulk_grid_of(int *grid, int *smem_bytes)
 {
     static std::atomic<int> cache[64], cache_smem[64];
@@ -373,7 +538,6 @@ cudaError_t bulk_grid_of(int *grid, int *smem_bytes)
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int v = cache[dev].load(std::memory_order_acquire);
     if (v <= 0) {
-        using Sh = BulkShape<W, MODE>;
         e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM);
         if (e != cudaSuccess) return e;
         int sms = 0, per_sm = 0;
@@ -413,7 +577,7 @@ cudaError_t launch_bulk_fixed(const LaunchSpec &s, int64_t head, cudaStream_t st
     p.do_scale = s.do_scale;
     p.pdl = DETFOLD_PDL_ALL ? 1 : 0;
     int cap = 0, smem = 0;
-    cudaError_t e = bulk_grid_of<fold_bulk_kernel<W, MODE>, W, MODE>(&cap, &smem);
+    cudaError_t e = bulk_grid_of<fold_bulk_kernel<W, MODE>, BulkShape<W, MODE>>(&cap, &smem);
     if (e != cudaSuccess) return e;
     int64_t grid = p.ntiles < cap ? p.ntiles : cap;
     if (grid < 1) grid = 1;
@@ -437,7 +601,7 @@ cudaError_t launch_bulk_table_fixed(const BulkTableParams &tp, cudaStream_t stre
 {
     using Sh = BulkShape<W, MODE>;
     int cap = 0, smem = 0;
-    cudaError_t e = bulk_grid_of<fold_bulk_table_kernel<W, MODE>, W, MODE>(&cap, &smem);
+    cudaError_t e = bulk_grid_of<fold_bulk_table_kernel<W, MODE>, BulkShape<W, MODE>>(&cap, &smem);
     if (e != cudaSuccess) return e;
     int64_t grid = tp.len / Sh::T;  // about one CTA per tile, at most the resident CTAs
     if (grid > cap) grid = cap;
@@ -455,6 +619,43 @@ cudaError_t launch_bulk_table_fixed(const BulkTableParams &tp, cudaStream_t stre
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, fold_bulk_table_kernel<W, MODE>, tp);
+}
+
+template <int W>
+cudaError_t launch_bulk_mixed_fixed(const LaunchSpec &s, cudaStream_t stream)
+{
+    using Sh = MixedShape<W>;
+    MixedParams<W> p = {};
+    const int64_t head0 = (4 - elem_phase(s.src[0], 4)) % 4;
+    p.base = head0 + 4;
+    p.len = s.len;
+    p.ntiles = s.len >= p.base + 4 + Sh::T ? (s.len - p.base - 4) / Sh::T : 0;
+    for (int r = 0; r < W; ++r) {
+        p.a[r] = const_cast<float *>(s.src[r]);
+        p.p[r] = elem_phase(s.src[r] + p.base, 4);
+        p.qmask |= 1 << ((4 - p.p[r]) & 3);
+    }
+    p.scale = s.scale;
+    p.do_scale = s.do_scale;
+    p.pdl = DETFOLD_PDL_ALL ? 1 : 0;
+    int cap = 0, smem = 0;
+    cudaError_t e = bulk_grid_of<fold_bulk_mixed_kernel<W>, Sh>(&cap, &smem);
+    if (e != cudaSuccess) return e;
+    int64_t grid = p.ntiles < cap ? p.ntiles : cap;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(Sh::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fold_bulk_mixed_kernel<W>, p);
 }
 
 template <int MODE>
@@ -524,6 +725,20 @@ cudaError_t launch_bulk_table(const float *const *d_table, float *out, int *d_st
     tp.pdl = DETFOLD_PDL_ALL ? 1 : 0;
     if (mode == kAllReduce) return launch_bulk_table_mode<kAllReduce>(tp, W, stream);
     return launch_bulk_table_mode<kSumCoherent>(tp, W, stream);
+}
+
+cudaError_t launch_bulk_mixed(const LaunchSpec &s, cudaStream_t stream)
+{
+    switch (s.W) {
+    case 1: return launch_bulk_mixed_fixed<1>(s, stream);
+    case 2: return launch_bulk_mixed_fixed<2>(s, stream);
+    case 3: return launch_bulk_mixed_fixed<3>(s, stream);
+    case 4: return launch_bulk_mixed_fixed<4>(s, stream);
+    case 5: return launch_bulk_mixed_fixed<5>(s, stream);
+    case 6: return launch_bulk_mixed_fixed<6>(s, stream);
+    case 7: return launch_bulk_mixed_fixed<7>(s, stream);
+    default: return launch_bulk_mixed_fixed<8>(s, stream);
+    }
 }
 
 cudaError_t launch_bulk(const LaunchSpec &s, int64_t head, cudaStream_t stream)

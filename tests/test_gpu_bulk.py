@@ -23,6 +23,29 @@ pytestmark = [pytest.mark.gpu,
 M = 1 << 21  # the fold's bulk-async threshold (DETFOLD_BULK_MIN_LEN)
 
 
+@pytest.mark.parametrize("W", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("n", [M, M + 1, M + 4099, 3 * M + 12345])
+def test_bulk_allreduce_arenas_at_different_16_byte_phases(W, n):
+    # The all-reduce whose arenas do not share a 16-byte phase takes the
+    # bulk-async pipeline with per-arena offsets at these sizes: each arena
+    # must end with the oracle's bits, guard bands intact, no wait expired.
+    rng = np.random.default_rng(31 * W + n % 1009)
+    offs = [int(x) for x in rng.integers(0, 8, size=W)]
+    if len({o % 4 for o in offs}) == 1:
+        offs[-1] = (offs[-1] + 1) % 8  # at least two 16-byte phases
+    rows = gen.stress_rows(W, n, seed0=int(rng.integers(1, 1 << 30)))
+    scale = float(oracle.mean_scale(W))
+    arenas = [Guarded(n, offs[r], rows[r]) for r in range(W)]
+    df.detfold_loopback_allreduce([a.t for a in arenas], W, n, scale)
+    torch.cuda.synchronize()
+    want = [rows[r].copy() for r in range(W)]
+    oracle.allreduce(want, np.float32(scale))
+    for r in range(W):
+        assert arenas[r].intact(), f"guard band of arena {r} (offsets {offs})"
+        assert_bitwise(arenas[r].host(), want[r], f"mixed-phase bulk all-reduce W={W} n={n} offs={offs} rank {r}")
+    assert df.detfold_pipeline_timeouts() == 0
+
+
 @pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("n", [M, M + 1, M + 2047, M + 4099, 3 * M + 12345])
 def test_bulk_sum_and_allreduce(W, n):

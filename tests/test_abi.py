@@ -67,9 +67,9 @@ def test_header_declares_the_api():
     assert set(declared_functions(PROBES_HEADER)) == PROBES_API
 
 
-def test_boundary_signatures_follow_the_scope_table():
-    # the calls of the boundary, with the argument order the hot-path scope
-    # gives them: (out, inputs, W, len, ..., stream)
+def test_boundary_signatures_are_pinned():
+    # the hot-path calls of the boundary and their argument order:
+    # (out, inputs, W, len, ..., stream)
     assert declaration("detfold_sum_stacked") == [
         ("float*", "out"), ("const float*", "stacked"), ("int", "W"), ("int64_t", "len"), ("void*", "stream")]
     assert declaration("detfold_sum_ptrs") == [

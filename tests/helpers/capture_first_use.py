@@ -1,5 +1,5 @@
-"""Run in a fresh process: the first use of the bulk-async, movement and
-realign kernels happens inside a CUDA-graph capture (their one-time set-up --
+"""Run in a fresh process: the first use of the bulk-async (aligned and
+mixed-phase), movement and realign kernels happens inside a CUDA-graph capture (their one-time set-up --
 shared-memory opt-in, occupancy -- runs during capture). Replays twice and
 writes the outputs for the parent test to check against the oracle."""
 import sys
@@ -18,6 +18,9 @@ st = torch.from_numpy(rows).cuda()
 out = torch.empty(n, device="cuda")
 arenas = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
 staged = [torch.from_numpy(rows[r]).cuda() for r in range(W)]
+# arenas at different 16-byte phases (3r mod 8 elements): the bulk all-reduce with per-arena offsets
+mixed_bufs = [torch.empty(n + 8, device="cuda") for _ in range(W)]
+mixed = [mixed_bufs[r][(3 * r) % 8:(3 * r) % 8 + n] for r in range(W)]
 nb = df.detfold_staged_workspace_bytes(n, W)
 ws = torch.empty(nb // 4, device="cuda")
 torch.cuda.synchronize()
@@ -28,13 +31,16 @@ with torch.cuda.graph(g, stream=s):
     df.detfold_sum_ptrs(out, [st[r] for r in range(W)], W, n)   # same; ptrs
     df.detfold_loopback_allreduce(arenas, W, n, 0.25)           # bulk all-reduce
     df.detfold_loopback_allreduce_staged(staged, W, n, 0.25, ws, nb)  # bulk moves + folds
+    df.detfold_loopback_allreduce(mixed, W, n, 0.25)            # bulk, mixed 16-byte phases
 for _ in range(2):
     for r in range(W):
         arenas[r].copy_(torch.from_numpy(rows[r]))
         staged[r].copy_(torch.from_numpy(rows[r]))
+        mixed[r].copy_(torch.from_numpy(rows[r]))
     g.replay()
 torch.cuda.synchronize()
 res = np.stack([out.cpu().numpy(), arenas[0].cpu().numpy(), arenas[W - 1].cpu().numpy(),
-                staged[0].cpu().numpy(), staged[W - 1].cpu().numpy()])
+                staged[0].cpu().numpy(), staged[W - 1].cpu().numpy(),
+                mixed[0].cpu().numpy(), mixed[W - 1].cpu().numpy()])
 np.save(out_path, res)
 print("timeouts", df.detfold_pipeline_timeouts())

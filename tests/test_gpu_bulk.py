@@ -169,5 +169,5 @@ def test_first_use_inside_graph_capture(tmp_path):
     assert_bitwise(res[0], oracle.fold(rows), "captured ptrs fold")
     want = [rows[q].copy() for q in range(W)]
     oracle.allreduce(want, np.float32(0.25))
-    for k, q in ((1, 0), (2, W - 1), (3, 0), (4, W - 1)):
+    for k, q in ((1, 0), (2, W - 1), (3, 0), (4, W - 1), (5, 0), (6, W - 1)):
         assert_bitwise(res[k], want[q], f"captured all-reduce result {k}")

@@ -74,6 +74,8 @@ def _cases():
     c["allreduce_bulk"] = lambda: allreduce(gen.stress_rows(3, M + 7), [1] * 3,
                                             float(oracle.mean_scale(3)))
     c["allreduce_small_mixed"] = lambda: allreduce(gen.normal_rows(5, 9999), [0, 1, 2, 3, 4], 1.0)
+    c["allreduce_bulk_mixed"] = lambda: allreduce(gen.stress_rows(4, M + 4099), [0, 3, 6, 1],
+                                                  float(oracle.mean_scale(4)))
 
     def staged(flags, W, n):
         k = Case(gen.normal_rows(W, n), [1] * W, n_out=1)

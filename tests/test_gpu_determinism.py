@@ -51,6 +51,15 @@ def test_every_entry_point_is_deterministic():
     scale = float(oracle.mean_scale(W))
     _ok(determinism_diff(lambda k: df.detfold_loopback_allreduce(arenas, W, N, scale),
                          lambda k: arenas, reset), "fused all-reduce")
+    # arenas at different 16-byte phases (the bulk pipeline with per-arena
+    # offsets at this length)
+    mixed = [Guarded(N, (3 * r) % 8, rows[r]) for r in range(W)]
+
+    def reset_mixed(k):
+        for m, s in zip(mixed, src):
+            m.t.copy_(s)
+    _ok(determinism_diff(lambda k: df.detfold_loopback_allreduce([m.t for m in mixed], W, N, scale),
+                         lambda k: [m.t for m in mixed], reset_mixed), "fused all-reduce, mixed phases")
     nb = df.detfold_staged_workspace_bytes(N, W)
     ws = torch.empty(nb // 4, device="cuda")
     for flags in (0, 1, 4, 7):

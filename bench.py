@@ -593,6 +593,79 @@ def next_rows(torch, df, wl, reps: int = 10, calls: int = 5) -> dict:
     return out
 
 
+def c5_launches(torch, df, wl, sets: int = 12, reps: int = 4, rounds: int = 2) -> dict:
+    """Device time per launch at the C5 length (2^20+7 at base + 4 B), each
+    of the row's three calls alone, beside torch's own elementwise kernels
+    at the same length (an add of two rows into a third; an in-place multiply
+    of one row). Each figure comes from a CUDA graph of `reps` x `sets`
+    back-to-back launches over `sets` buffer sets whose footprint exceeds L2,
+    so every launch reads cold data but none pays a host launch; median of 9
+    replays, the best of `rounds` interleaved rounds. At this length a
+    launch's fixed cost (the predecessor's retirement, the first DRAM round
+    trip, the ramp over the SMs) is comparable to its transfer time."""
+    dev, n = wl.dev, C5_N
+    stream = torch.cuda.Stream()
+
+    def per_launch_us(enq):
+        with torch.cuda.stream(stream):
+            for k in range(sets):
+                enq(k)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                for k in range(sets):
+                    enq(k)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(9):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record()
+                g.replay()
+                b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / (reps * sets))
+        del g
+        return statistics.median(ts)
+
+    calls, nbytes = {}, {}
+    for W in C5_WS:
+        bufs = []
+        for k in range(sets):
+            b = torch.empty((2 * W + 1, n + 1), dtype=torch.float32, device=dev)
+            for r in range(W):
+                b[r, 1:].copy_(wl.c5_sum_src[W][r])
+                b[W + r, 1:].copy_(wl.c5_sum_src[W][r])
+            bufs.append(([b[r, 1:] for r in range(W)], [b[W + r, 1:] for r in range(W)], b[2 * W, 1:]))
+        m = wl.scale5[W]
+        calls[f"w{W}_sum"] = lambda k, W=W, bufs=bufs: df.detfold_sum_ptrs(bufs[k][2], bufs[k][0], W, n)
+        calls[f"w{W}_mean_pass"] = lambda k, bufs=bufs, m=m: df.detfold_scale(bufs[k][2], n, m)
+        calls[f"w{W}_allreduce"] = lambda k, W=W, bufs=bufs, m=m: df.detfold_loopback_allreduce(
+            bufs[k][1], W, n, m)
+        nbytes[f"w{W}_sum"] = (W + 1) * n * 4
+        nbytes[f"w{W}_mean_pass"] = 2 * n * 4
+        nbytes[f"w{W}_allreduce"] = 2 * W * n * 4
+    tbufs = [torch.randn((3, n), device=dev) for _ in range(sets)]
+    calls["torch_add"] = lambda k: torch.add(tbufs[k][0], tbufs[k][1], out=tbufs[k][2])
+    calls["torch_mul_inplace"] = lambda k: tbufs[k][2].mul_(0.5)
+    nbytes["torch_add"] = 3 * n * 4
+    nbytes["torch_mul_inplace"] = 2 * n * 4
+    best = {}
+    for _ in range(rounds):
+        for key, fn in calls.items():
+            us = per_launch_us(fn)
+            best[key] = min(best.get(key, us), us)
+    out = {key: {"us": round(us, 3), "gbs": round(nbytes[key] / (us * 1e-6) / 1e9, 1)}
+           for key, us in best.items()}
+    out["timing"] = (f"graphs of {reps} x {sets} launches over {sets} buffer sets (cold data), "
+                     f"median of 9 replays, best of {rounds} rounds")
+    return out
+
+
 def arm_config(world: int) -> dict:
     """The workload both arms report: one pass of every hot-path row."""
     return {
@@ -928,6 +1001,7 @@ def run_gpu(args) -> None:
     graph = graph_us_per_call(torch, df, wl)
     graph_samples = graph.pop("_specs")
     extra_rows = next_rows(torch, df, wl)
+    c5_launch = c5_launches(torch, df, wl)
 
     # End to end through the public API with host buffers: every step copies
     # each row's inputs from pinned host memory, runs the row, and reads back
@@ -1122,6 +1196,7 @@ def run_gpu(args) -> None:
         "roofline": roofline,
         "c2_graph": graph,
         "next_rows": extra_rows,
+        "c5_launches": c5_launch,
         "copy_peak_gbs_this_run": round(copy_gbs, 1),
         "peaks_this_run": {"d2d_copy_gbs": round(peaks_run["d2d_copy_gbs"], 1),
                            "stream_kernel_gbs": round(peaks_run["stream_kernel_gbs"], 1),

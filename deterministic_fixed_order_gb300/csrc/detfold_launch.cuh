@@ -123,7 +123,8 @@ inline cudaError_t sm_count(int *out)
 // parameter block's pdl flag is set.
 template <auto Kernel, typename Params>
 inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool small, int bw_threads,
-                                 int cap_per_sm, cudaStream_t stream, bool fill = true)
+                                 int cap_per_sm, cudaStream_t stream, bool fill = true,
+                                 int extra_blocks = 0)
 {
     int threads = small ? DETFOLD_SMALL_THREADS : bw_threads;
     int64_t blocks = (work + threads - 1) / threads;
@@ -145,10 +146,12 @@ inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool smal
                 blocks = (work + per_iter - 1) / per_iter;
             }
         }
-        if (blocks > cap) blocks = cap;
+        // every CTA, the extra ones included, resident at once
+        if (blocks > cap - extra_blocks) blocks = cap - extra_blocks;
     }
     if (blocks < 1) blocks = 1;
-    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    if (blocks > 0x7FFFFFFF - extra_blocks) blocks = 0x7FFFFFFF - extra_blocks;
+    blocks += extra_blocks;  // CTAs with work of their own (a vector kernel's edge CTA)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
@@ -166,12 +169,14 @@ inline cudaError_t launch_kernel(const Params &p, int64_t work, int u, bool smal
     return cudaLaunchKernelEx(&cfg, Kernel, p);
 }
 
-// A small-path launch: ceil(work / threads) CTAs of `threads`, always with
-// programmatic dependent launch when the parameters ask for it.
+// A small-path launch: ceil(work / threads) CTAs of `threads` after
+// `extra_blocks` leading CTAs with work of their own (the edge CTA), always
+// with programmatic dependent launch when the parameters ask for it.
 template <auto Kernel, typename Params>
-inline cudaError_t launch_small(const Params &p, int64_t work, int threads, cudaStream_t stream)
+inline cudaError_t launch_small(const Params &p, int64_t work, int threads, cudaStream_t stream,
+                                int extra_blocks = 0)
 {
-    int64_t blocks = (work + threads - 1) / threads;
+    int64_t blocks = (work + threads - 1) / threads + extra_blocks;
     if (blocks < 1) blocks = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
@@ -231,12 +236,13 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
     if (small && pl.vec != 0) {
         // the fewest vectors take smaller CTAs, spread over more SMs
         const int threads = pl.nvec <= DETFOLD_TINY_VECS ? DETFOLD_TINY_THREADS : DETFOLD_SMALL_THREADS;
-        const bool exact = DETFOLD_SMALL_EXACT && pl.nvec > 0 && pl.nvec % threads == 0;
+        const bool exact = DETFOLD_SMALL_EXACT && pl.nvec > 0 && pl.nvec % threads == 0 && !p.edges;
+        const int e = p.edges;  // the edge CTA
         if (pl.vec == 8)
-            return exact ? launch_small<fold_small_kernel<W, 8, MODE, true>>(p, pl.nvec, threads, stream)
-                         : launch_small<fold_small_kernel<W, 8, MODE, false>>(p, pl.nvec, threads, stream);
-        return exact ? launch_small<fold_small_kernel<W, 4, MODE, true>>(p, pl.nvec, threads, stream)
-                     : launch_small<fold_small_kernel<W, 4, MODE, false>>(p, pl.nvec, threads, stream);
+            return exact ? launch_small<fold_small_kernel<W, 8, MODE, true>>(p, pl.nvec, threads, stream, e)
+                         : launch_small<fold_small_kernel<W, 8, MODE, false>>(p, pl.nvec, threads, stream, e);
+        return exact ? launch_small<fold_small_kernel<W, 4, MODE, true>>(p, pl.nvec, threads, stream, e)
+                     : launch_small<fold_small_kernel<W, 4, MODE, false>>(p, pl.nvec, threads, stream, e);
     }
     // a vector kernel whose CTA was shrunk to fit its registers gets as many
     // more CTAs per SM as the cap allows, so the threads per SM stay the same
@@ -273,8 +279,9 @@ inline cudaError_t launch_fixed(const LaunchSpec &s, cudaStream_t stream)
         q.scale = s.scale;
         q.do_scale = s.do_scale;
         q.pdl = p.pdl;
-        // a warp covers 31 vectors per pass, DETFOLD_REALIGN_U passes per iteration
-        const int64_t work = q.nvec > 2 ? (q.nvec - 2 + 30) / 31 * 32 : 32;
+        // a warp covers 31 vectors per pass, DETFOLD_REALIGN_U passes per
+        // iteration; one warp more, with no pass, folds the scalar edges
+        const int64_t work = (q.nvec > 2 ? (q.nvec - 2 + 30) / 31 * 32 : 0) + 32;
         static_assert(DETFOLD_SMALL_THREADS <= DETFOLD_REALIGN_THREADS, "small launches fit the launch bound");
         // (its CTA size stays: smaller CTAs measured slower for this kernel)
         return launch_kernel<fold_realign_kernel<W, MODE>>(q, work, DETFOLD_REALIGN_U, small,

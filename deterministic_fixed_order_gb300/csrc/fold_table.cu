@@ -209,7 +209,7 @@ __device__ __forceinline__ void table_fixed_vec(const TableParams &p, const floa
     }
 }
 
-// The W entries of a small call, passed by value to the out-of-line parts.
+// The W entries of a small call, held in registers.
 template <int WT>
 struct SrcSet {
     const float *p[WT];
@@ -231,11 +231,13 @@ __device__ __forceinline__ void table_fold_one(const TableParams &p, const SrcSe
     }
 }
 
+// Thread i < 8 folds head element i, thread 8 + j tail element j (inline,
+// as the fold's own small kernel does).
 template <int WT, int MODE>
-__device__ __noinline__ void table_small_edges(const TableParams &p, SrcSet<WT> s, int i, int head, int tail0)
+__device__ __forceinline__ void table_small_edges(const TableParams &p, SrcSet<WT> s, int i, int head, int tail0)
 {
-    if (i < head) table_fold_one<WT, MODE>(p, s, i);
-    if (i < (int)p.len - tail0) table_fold_one<WT, MODE>(p, s, tail0 + i);
+    if (i < 8 ? i < head : i - 8 < (int)p.len - tail0)
+        table_fold_one<WT, MODE>(p, s, i < 8 ? i : tail0 + (i - 8));
 }
 
 // A small call whose entries share no 32-byte phase: 16-byte vectors if
@@ -256,9 +258,9 @@ __device__ __noinline__ void table_small_slow(const TableParams &p, SrcSet<WT> s
 // no shared memory and no block barrier between the table load and the data
 // loads. The common case, every entry (and the output) at one 32-byte phase,
 // is one 32-byte vector per thread with 32-bit indices; the head and tail
-// and the narrower widths run out of line, so the code a CTA executes after
-// the wait -- what the latency of a graph of small folds is made of -- stays
-// short.
+// run in a leading CTA of their own and the narrower widths out of line, so
+// the code a CTA executes after the wait -- what the latency of a graph of
+// small folds is made of -- stays short.
 template <int WT, int MODE>
 __global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) fold_table_small_kernel(const __grid_constant__ TableParams p)
 {
@@ -288,7 +290,16 @@ __global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) fold_table_small_kernel
     int head = (int)(((32u - ph0) & 31u) / 4);
     if (head > len) head = len;
     const int nvec = (len - head) / 8;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int tail0 = head + nvec * 8;
+    // the first CTA folds the head and the tail alone (the host always adds
+    // it: only the device sees the entries' phases), so their memory round
+    // trip runs beside the vectors' instead of after one thread's vector
+    if (blockIdx.x == 0) {
+        if ((head != 0 || tail0 != len) && threadIdx.x < 16)
+            table_small_edges<WT, MODE>(p, s, threadIdx.x, head, tail0);
+        return;
+    }
+    const int i = (blockIdx.x - 1) * blockDim.x + threadIdx.x;
     if (i < nvec) {
         const int e = head + i * 8;
         Vec<8> x[WT];
@@ -310,16 +321,15 @@ __global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) fold_table_small_kernel
             stv<8>(p.out + e, acc);
         }
     }
-    const int tail0 = head + nvec * 8;
-    if ((head != 0 || tail0 != len) && i < 8) table_small_edges<WT, MODE>(p, s, i, head, tail0);
 }
 
 template <int WT>
 cudaError_t launch_table_small(const TableParams &p, int64_t work, int mode, cudaStream_t stream)
 {
+    // one leading CTA for the edges (fold_table_small_kernel)
     if (mode == kAllReduce)
-        return launch_kernel<fold_table_small_kernel<WT, kAllReduce>>(p, work, 1, true, 256, 0, stream);
-    return launch_kernel<fold_table_small_kernel<WT, kSumCoherent>>(p, work, 1, true, 256, 0, stream);
+        return launch_kernel<fold_table_small_kernel<WT, kAllReduce>>(p, work, 1, true, 256, 0, stream, true, 1);
+    return launch_kernel<fold_table_small_kernel<WT, kSumCoherent>>(p, work, 1, true, 256, 0, stream, true, 1);
 }
 
 }  // namespace

@@ -196,13 +196,46 @@ cudaError_t launch_move_bulk_fixed(const float *const *src, float *const *dst, i
     return cudaLaunchKernelEx(&cfg, move_bulk_kernel<G>, p);
 }
 
+// The head and tail elements of every pair (fewer than VEC each), run by
+// the launch's leading p.edge_blocks CTAs, so their memory round trips run
+// beside the vectors' instead of after them. Element j of the K * nedge
+// numbers pair j / nedge; thread `i` takes j = i, i + step, ..., four loads
+// ahead of their stores.
+template <int VEC>
+__device__ __forceinline__ void move_edges(const MoveParams &p, int i, int step)
+{
+    const int nedge = (int)(p.len - p.nvec * VEC);  // head + tail
+    const int64_t tail0 = p.head + p.nvec * VEC;
+    const int n = p.K * nedge;
+    for (; i < n; i += 4 * step) {
+        float x[4];
+        int64_t e[4];
+        int k[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = i + u * step;
+            k[u] = j < n ? j / nedge : 0;
+            const int q = j - k[u] * nedge;
+            e[u] = q < (int)p.head ? q : tail0 + (q - (int)p.head);
+            if (j < n) x[u] = ld1<true>(p.src[k[u]] + e[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i + u * step < n) st1(p.dst[k[u]] + e[u], x[u]);
+    }
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(256) move_pairs_kernel(const __grid_constant__ MoveParams p)
 {
     constexpr int G = 4;
     pdl_enter(p.pdl);
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if ((int)blockIdx.x < p.edge_blocks) {
+        move_edges<VEC>(p, blockIdx.x * blockDim.x + threadIdx.x, p.edge_blocks * blockDim.x);
+        return;
+    }
+    const int64_t stride = (int64_t)(gridDim.x - p.edge_blocks) * blockDim.x;
+    const int64_t gtid = (int64_t)(blockIdx.x - p.edge_blocks) * blockDim.x + threadIdx.x;
     for (int64_t v = gtid; v < p.nvec; v += stride) {
         const int64_t e = p.head + v * VEC;
         Vec<VEC> x[G];
@@ -222,45 +255,34 @@ __global__ void __launch_bounds__(256) move_pairs_kernel(const __grid_constant__
                 if (k0 + k < p.K) stv<VEC>(p.dst[k0 + k] + e, x[k]);
         }
     }
-    // head and tail elements (fewer than VEC each)
-    const int64_t tail0 = p.head + p.nvec * VEC;
-    const int64_t ntail = p.len - tail0;
-    for (int part = 0; part < 2; ++part) {
-        const int64_t i = part == 0 ? gtid : tail0 + gtid;
-        if ((part == 0 && gtid < p.head) || (part == 1 && gtid < ntail)) {
-            for (int k = 0; k < p.K; ++k) st1(p.dst[k] + i, ld1<true>(p.src[k] + i));
-        }
-    }
-}
-
-// The head and tail elements of a small move (fewer than VEC each per pair),
-// out of line: thread i < K * (head + tail) moves one element of one pair.
-__device__ __noinline__ void move_small_edges(const MoveParams &p, int i, int nedge, int tail0)
-{
-    const int k = i / nedge, q = i - k * nedge;
-    const int e = q < (int)p.head ? q : tail0 + (q - (int)p.head);
-    st1(p.dst[k] + e, ld1<true>(p.src[k] + e));
 }
 
 // Small moves (len <= DETFOLD_SMALL_LEN, every pointer at one phase): one
 // (pair, vector) per thread with 32-bit indices, so a call is one dependent
 // load and store, not one per group of pairs as in the looping kernel above.
 // Pairs that share a source load it separately (from L2, at these sizes).
-template <int VEC>
+// EDGES: the call has a head or a tail, moved by the leading p.edge_blocks
+// CTAs (one element per thread); without, the kernel has no edge code.
+template <int VEC, bool EDGES>
 __global__ void __launch_bounds__(DETFOLD_SMALL_THREADS) move_small_kernel(const __grid_constant__ MoveParams p)
 {
     static_assert((int64_t)DETFOLD_SMALL_LEN * kMaxPairs < (1LL << 31), "small-move indices are 32-bit");
     pdl_enter(p.pdl);
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    int b = blockIdx.x;
+    if constexpr (EDGES) {
+        if (b < p.edge_blocks) {
+            move_edges<VEC>(p, b * blockDim.x + threadIdx.x, p.edge_blocks * blockDim.x);
+            return;
+        }
+        b -= p.edge_blocks;
+    }
+    const int i = b * blockDim.x + threadIdx.x;
     const int nvec = (int)p.nvec;
     if (i < p.K * nvec) {
         const int k = i / nvec;
         const int e = (int)p.head + (i - k * nvec) * VEC;
         stv<VEC>(p.dst[k] + e, ldv<VEC, true>(p.src[k] + e));
     }
-    const int tail0 = (int)p.head + nvec * VEC;
-    const int nedge = (int)p.len - nvec * VEC;  // head + tail
-    if (nedge > 0 && i < p.K * nedge) move_small_edges(p, i, nedge, tail0);
 }
 
 // Operands at different 4-byte phases: coalesced scalar moves.
@@ -330,16 +352,22 @@ static cudaError_t launch_move_chunk(const float *const *src, float *const *dst,
             break;
         }
     }
+    const int64_t edges = vec ? (int64_t)K * (len - p.nvec * vec) : 0;  // head + tail elements
     if (small && vec != 0) {
-        // one thread per (pair, vector), and enough threads for the edges
-        int64_t work = (int64_t)K * p.nvec;
-        const int64_t edges = (int64_t)K * (len - p.nvec * vec);
-        if (edges > work) work = edges;
-        if (vec == 8) return launch_kernel<move_small_kernel<8>>(p, work, 1, true, 256, 0, stream);
-        return launch_kernel<move_small_kernel<4>>(p, work, 1, true, 256, 0, stream);
+        // one thread per (pair, vector), after leading CTAs with one thread
+        // per edge element
+        p.edge_blocks = (short)((edges + DETFOLD_SMALL_THREADS - 1) / DETFOLD_SMALL_THREADS);  // <= 28
+        const int64_t work = (int64_t)K * p.nvec;
+        const int eb = p.edge_blocks;
+        if (vec == 8)
+            return eb ? launch_kernel<move_small_kernel<8, true>>(p, work, 1, true, 256, 0, stream, true, eb)
+                      : launch_kernel<move_small_kernel<8, false>>(p, work, 1, true, 256, 0, stream);
+        return eb ? launch_kernel<move_small_kernel<4, true>>(p, work, 1, true, 256, 0, stream, true, eb)
+                  : launch_kernel<move_small_kernel<4, false>>(p, work, 1, true, 256, 0, stream);
     }
-    if (vec == 8) return launch_kernel<move_pairs_kernel<8>>(p, p.nvec, 1, small, 256, 0, stream);
-    if (vec == 4) return launch_kernel<move_pairs_kernel<4>>(p, p.nvec, 1, small, 256, 0, stream);
+    p.edge_blocks = edges > 0 ? 1 : 0;
+    if (vec == 8) return launch_kernel<move_pairs_kernel<8>>(p, p.nvec, 1, small, 256, 0, stream, true, p.edge_blocks);
+    if (vec == 4) return launch_kernel<move_pairs_kernel<4>>(p, p.nvec, 1, small, 256, 0, stream, true, p.edge_blocks);
     return launch_kernel<move_pairs_scalar_kernel>(p, len, 1, small, 256, 0, stream);
 }
 

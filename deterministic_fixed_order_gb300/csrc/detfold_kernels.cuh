@@ -53,6 +53,9 @@
 #ifndef DETFOLD_AR_INFLIGHT
 #define DETFOLD_AR_INFLIGHT 256  // the same for the all-reduce mode
 #endif
+#ifndef DETFOLD_SCALE_INFLIGHT
+#define DETFOLD_SCALE_INFLIGHT 512  // the same for the W=1 scale pass (the mean pass)
+#endif
 #ifndef DETFOLD_SUM_MAX_FLOATS
 #define DETFOLD_SUM_MAX_FLOATS 32  // cap on loaded floats per thread per group (U > 1), sum modes
 #endif

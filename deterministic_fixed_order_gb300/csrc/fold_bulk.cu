@@ -451,6 +451,7 @@ struct MixedShape {
     static constexpr int THREADS = 32 * (1 + NCW);
     static constexpr size_t SMEM = (size_t)S * W * TL * 4 + (size_t)S * 4 * T * 4 + 2 * S * 8;
     static_assert(T % 4 == 0 && T >= 8, "tiles of whole 16-byte units, with an interior");
+    static_assert(W > 6 || T % (4 * 32 * NCW) == 0, "the consumers cover a tile in whole passes of 4 elements per thread");
     static_assert(8 * W <= 32 * NCW, "one consumer thread per partial element");
 };
 
@@ -515,26 +516,62 @@ __global__ void __launch_bounds__(MixedShape<W>::THREADS) fold_bulk_mixed_kernel
         if (named_sync_any(1, NC, !landed)) break;
         const float *src = in + (size_t)s * W * TL;
         float *rq = res + (size_t)s * 4 * T;
-        for (int j = tc * 4; j < T; j += NC * 4) {
-            float acc[4];
+        if constexpr (W <= 6) {
+            // thread tc takes elements e0 + tc + m * NC: a warp's shared loads
+            // and stores are 32 consecutive words, free of bank conflicts
+            // whatever the arena's phase offset (measured 0.4-3.9% faster
+            // for W = 2..6 at 2^24 per arena)
+            for (int e0 = 0; e0 < T; e0 += NC * 4) {
+                float acc[4];
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) acc[kk] = src[p.p[0] + j + kk];
+                for (int m = 0; m < 4; ++m) acc[m] = src[p.p[0] + e0 + m * NC + tc];
 #pragma unroll
-            for (int r = 1; r < W; ++r)
+                for (int r = 1; r < W; ++r)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) acc[kk] = __fadd_rn(acc[kk], src[(size_t)r * TL + p.p[r] + j + kk]);
-            if (p.do_scale) {
+                    for (int m = 0; m < 4; ++m)
+                        acc[m] = __fadd_rn(acc[m], src[(size_t)r * TL + p.p[r] + e0 + m * NC + tc]);
+                if (p.do_scale) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) acc[kk] = __fmul_rn(acc[kk], p.scale);
+                    for (int m = 0; m < 4; ++m) acc[m] = __fmul_rn(acc[m], p.scale);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) rq[e0 + m * NC + tc] = acc[m];
+#pragma unroll
+                for (int q = 1; q < 4; ++q) {
+                    if (p.qmask & (1 << q)) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int e = e0 + m * NC + tc;  // copy q holds elements q .. T-5+q
+                            if (e >= q && e < T - 4 + q) rq[q * T + e - q] = acc[m];
+                        }
+                    }
+                }
             }
-            *(float4 *)(rq + j) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        } else {
+            // W = 7, 8: four consecutive elements per thread and one 16-byte
+            // store of copy 0 (measured 1.3-2.2% faster here than the layout
+            // above, despite its 4-way bank conflicts)
+            for (int j = tc * 4; j < T; j += NC * 4) {
+                float acc[4];
 #pragma unroll
-            for (int q = 1; q < 4; ++q) {
-                if (p.qmask & (1 << q)) {
+                for (int kk = 0; kk < 4; ++kk) acc[kk] = src[p.p[0] + j + kk];
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const int e = j + kk;  // copy q holds elements q .. T-5+q
-                        if (e >= q && e < T - 4 + q) rq[q * T + e - q] = acc[kk];
+                for (int r = 1; r < W; ++r)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) acc[kk] = __fadd_rn(acc[kk], src[(size_t)r * TL + p.p[r] + j + kk]);
+                if (p.do_scale) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) acc[kk] = __fmul_rn(acc[kk], p.scale);
+                }
+                *(float4 *)(rq + j) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+                for (int q = 1; q < 4; ++q) {
+                    if (p.qmask & (1 << q)) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int e = j + kk;  // copy q holds elements q .. T-5+q
+                            if (e >= q && e < T - 4 + q) rq[q * T + e - q] = acc[kk];
+                        }
                     }
                 }
             }

@@ -64,11 +64,11 @@ E2E_PASSES = 5  # end-to-end passes; `e2e.value` is their median
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147525632 + 259119360,
-                                  "kernel_hash": "beea9629de214664"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147519744 + 259219968,
+                                  "kernel_hash": "5d5713eca1af968e"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600032000 + 1539115776,
-                                         "kernel_hash": "beea9629de214664"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600109056 + 1538207744,
+                                         "kernel_hash": "5d5713eca1af968e"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",

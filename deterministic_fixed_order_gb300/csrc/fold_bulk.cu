@@ -83,21 +83,44 @@ namespace {
 // All-reduce shapes per W (floats per rank per tile, stages, CTAs per SM),
 // from an interleaved A/B sweep on GB300 against the sums' shapes (same
 // bits): W=2 +5%, W=3 +3%, W=4 +2-3% (the 4 x 1e8 call 6.47 -> 6.61 TB/s),
-// W=8 +6%. W=1 and W=5-6 measured faster with the sums' shapes and keep them.
+// W=8 +6%. W=5-6 measured faster with the sums' shapes and keep them; W=1
+// has its own (below).
+// The W=1 all-reduce (a scale pass) takes the W=1 sum's deep shape below:
+// 6.81 TB/s at 1 GiB against 6.62 with 8 KB tiles in 3 stages at 2 CTAs per SM.
+#ifndef DETFOLD_BULK_AR_W1_T
+#define DETFOLD_BULK_AR_W1_T 4096  // floats per tile,
+#endif
+#ifndef DETFOLD_BULK_AR_W1_S
+#define DETFOLD_BULK_AR_W1_S 4     // stages,
+#endif
+#ifndef DETFOLD_BULK_AR_W1_C
+#define DETFOLD_BULK_AR_W1_C 1     // CTAs per SM
+#endif
 template <int W>
 struct ArShape {
-    static constexpr int T = W == 1 ? 2048 : W <= 3 ? 1024 : W == 4 ? 512 : W <= 6 ? 1024 : 256;
-    static constexpr int S = W == 1 ? 3 : W <= 3 ? 2 : W == 4 ? 3 : W <= 6 ? 2 : 3;
-    static constexpr int C = W <= 3 && W > 1 ? 3 : 2;
+    static constexpr int T = W == 1 ? DETFOLD_BULK_AR_W1_T : W <= 3 ? 1024 : W == 4 ? 512 : W <= 6 ? 1024 : 256;
+    static constexpr int S = W == 1 ? DETFOLD_BULK_AR_W1_S : W <= 3 ? 2 : W == 4 ? 3 : W <= 6 ? 2 : 3;
+    static constexpr int C = W == 1 ? DETFOLD_BULK_AR_W1_C : W <= 3 ? 3 : 2;
 };
+// The W=1 sum (a 1:1 stream) keeps more bytes in flight than the other sums:
+// 16 KB tiles in 4 stages (one CTA per SM) measured 6.83 TB/s at 1 GiB
+// against 5.84 with the shared 4 KB shape, and 6.60 for a torch device copy.
+#ifndef DETFOLD_BULK_SUM_W1_T
+#define DETFOLD_BULK_SUM_W1_T 4096
+#endif
+#ifndef DETFOLD_BULK_SUM_W1_S
+#define DETFOLD_BULK_SUM_W1_S 4
+#endif
 template <int W, int MODE>
 struct BulkShape {
     static constexpr bool AR = (MODE == kAllReduce);
     static constexpr bool PER_W = AR && DETFOLD_BULK_AR_PER_W;
     static constexpr int T = PER_W ? ArShape<W>::T
+                           : (!AR && W == 1) ? DETFOLD_BULK_SUM_W1_T
                            : W <= 4 ? (AR ? DETFOLD_BULK_AR_T_LO : DETFOLD_BULK_T_LO)
                                     : (AR ? DETFOLD_BULK_AR_T_HI : DETFOLD_BULK_T_HI);
     static constexpr int S = PER_W ? ArShape<W>::S
+                           : (!AR && W == 1) ? DETFOLD_BULK_SUM_W1_S
                            : W <= 4 ? (AR ? DETFOLD_BULK_AR_S_LO : DETFOLD_BULK_S_LO)
                                     : (AR ? DETFOLD_BULK_AR_S_HI : DETFOLD_BULK_S_HI);
     static constexpr int CTAS_PER_SM = PER_W ? ArShape<W>::C

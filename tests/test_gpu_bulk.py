@@ -85,6 +85,22 @@ def test_bulk_sum_and_allreduce(W, n):
         assert arenas[r].intact()
 
 
+@pytest.mark.parametrize("n", [M, M + 4099, 3 * M + 12345])
+@pytest.mark.parametrize("off", [0, 1, 2, 3])
+def test_bulk_scale_pass_matches_the_oracle(n, off):
+    # The separate mean pass at bulk sizes (a W=1 all-reduce on the bulk
+    # pipeline, with its own deeper tile shape): fl(x * s) element by element,
+    # at every 16-byte phase of the buffer, guard bands intact.
+    row = gen.stress_rows(1, n, seed0=5 + off)[0]
+    s = float(oracle.mean_scale(3))
+    buf = Guarded(n, off, row)
+    df.detfold_scale(buf.t, n, s)
+    torch.cuda.synchronize()
+    assert buf.intact()
+    assert_bitwise(buf.host(), oracle.scale(row, s), f"scale n={n} off={off}")
+    assert df.detfold_pipeline_timeouts() == 0
+
+
 def test_bulk_repeated_calls_and_no_pipeline_timeouts():
     W, n = 4, 5 * M + 777
     rows = gen.normal_rows(W, n)

@@ -64,15 +64,16 @@ E2E_PASSES = 5  # end-to-end passes; `e2e.value` is their median
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147519744 + 259219968,
-                                  "kernel_hash": "5d5713eca1af968e"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147640064 + 259569664,
+                                  "kernel_hash": "49dc394bce5c6240"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600109056 + 1538207744,
-                                         "kernel_hash": "5d5713eca1af968e"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600091904 + 1538560000,
+                                         "kernel_hash": "49dc394bce5c6240"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",
-                "fold_sum_coherent.cu", "fold_allreduce.cu", "fold_bulk.cu")
+                "fold_sum_coherent.cu", "fold_allreduce.cu", "fold_bulk.cu", "fold_table.cu",
+                "move_kernels.cu", "one_shot.cu")
 
 
 def _code_only(text: str) -> str:
@@ -83,7 +84,7 @@ def _code_only(text: str) -> str:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the fold kernels and their launch configuration (code only:
+    """Hash of every kernel source and its launch configuration (code only:
     editing a comment does not invalidate a profile)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "deterministic_fixed_order_gb300", "csrc")

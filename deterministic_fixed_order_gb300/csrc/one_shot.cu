@@ -44,6 +44,8 @@ namespace {
 
 constexpr int kOneShotThreads = 256;
 constexpr unsigned kMaxPolls = 1u << 26;  // hard cap on polls of one wait
+constexpr int kU = 4;                     // elements per thread per group
+constexpr int kFastW = 8;                 // worlds up to this size load a group ahead
 
 struct OneShotParams {
     float *arena[DETFOLD_ONESHOT_MAX_W];
@@ -105,7 +107,7 @@ __device__ bool cta_barrier(unsigned long long *flags, int nctas, unsigned long 
             }
             // the expiry decision must be the same in every lane of the warp
             if (__any_sync(0xffffffffu, global_ns() - t0 > wait_ns)) break;
-            __nanosleep(200);
+            __nanosleep(32);
         }
         if (threadIdx.x == 0) s_ok = ok ? 1 : 0;
     }
@@ -141,14 +143,46 @@ __global__ void __launch_bounds__(kOneShotThreads) one_shot_kernel(const __grid_
         return;  // x untouched
     }
 
-    // 2. rank r folds every arena into its stage row (its CTAs split the row)
+    // 2. rank r folds every arena into its stage row (its CTAs split the
+    // row). A thread's elements i, i + stride, ... go kU at a time; up to
+    // kFastW ranks, every load of the group is issued before the first add
+    // (one memory round trip per group, not one per element). The chain of
+    // each element stays in ascending rank order.
     float *stage = p.stage + (int64_t)r * p.len;
     const int64_t stride = (int64_t)p.ctas_per_rank * blockDim.x;
-    for (int64_t i = (int64_t)g * blockDim.x + threadIdx.x; i < p.len; i += stride) {
-        float acc = ld1<false>(p.arena[0] + i);
-        for (int q = 1; q < p.W; ++q) acc = __fadd_rn(acc, ld1<false>(p.arena[q] + i));
-        if (p.do_scale) acc = __fmul_rn(acc, p.scale);
-        st1(stage + i, acc);
+    for (int64_t i0 = (int64_t)g * blockDim.x + threadIdx.x; i0 < p.len; i0 += kU * stride) {
+        if (p.W <= kFastW) {
+            float x[kU][kFastW];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = i0 + u * stride;
+#pragma unroll
+                for (int q = 0; q < kFastW; ++q)
+                    if (q < p.W && i < p.len) x[u][q] = ld1<false>(p.arena[q] + i);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = i0 + u * stride;
+                if (i < p.len) {
+                    float acc = x[u][0];
+#pragma unroll
+                    for (int q = 1; q < kFastW; ++q)
+                        if (q < p.W) acc = __fadd_rn(acc, x[u][q]);
+                    if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+                    st1(stage + i, acc);
+                }
+            }
+        } else {
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = i0 + u * stride;
+                if (i < p.len) {
+                    float acc = ld1<false>(p.arena[0] + i);
+                    for (int q = 1; q < p.W; ++q) acc = __fadd_rn(acc, ld1<false>(p.arena[q] + i));
+                    if (p.do_scale) acc = __fmul_rn(acc, p.scale);
+                    st1(stage + i, acc);
+                }
+            }
+        }
     }
 
     // 3. exit barrier: every rank has finished reading the arenas
@@ -162,9 +196,17 @@ __global__ void __launch_bounds__(kOneShotThreads) one_shot_kernel(const __grid_
         return;  // x untouched
     }
 
-    // 4. the stage row becomes the arena
-    for (int64_t i = (int64_t)g * blockDim.x + threadIdx.x; i < p.len; i += stride)
-        st1(p.arena[r] + i, ld1<false>(stage + i));
+    // 4. the stage row becomes the arena (the elements this thread staged,
+    // kU loads ahead of their stores)
+    for (int64_t i0 = (int64_t)g * blockDim.x + threadIdx.x; i0 < p.len; i0 += kU * stride) {
+        float y[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (i0 + u * stride < p.len) y[u] = ld1<false>(stage + i0 + u * stride);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (i0 + u * stride < p.len) st1(p.arena[r] + i0 + u * stride, y[u]);
+    }
     raise_counter(p, epoch);
 }
 

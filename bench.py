@@ -1006,8 +1006,9 @@ def run_gpu(args) -> None:
 
     # End to end through the public API with host buffers: every step copies
     # the step's inputs from pinned host memory, runs every row, and reads
-    # back every result. The C4 input crosses the link once; the staged row
-    # gets its in-place copy of it on the device (dup_rows). Three streams pipeline the rows: uploads run ahead on an
+    # back every result. Every input crosses the link once: a row that folds
+    # in place an input another call also reads gets its copy on the device
+    # (dup_rows). Three streams pipeline the rows: uploads run ahead on an
     # H2D stream, the calls run on the compute stream as each row's inputs
     # land, and results drain on a D2H stream, so the two link directions
     # overlap. Events keep a buffer from being overwritten before the previous
@@ -1034,10 +1035,11 @@ def run_gpu(args) -> None:
             "c4_staged": ([], [(h_out["c4s"][r * C4_N:(r + 1) * C4_N], w.c4s[r]) for r in range(C4_W)]),
         }
         for W in C5_WS:
+            # the sum's sources cross the link; the all-reduce's arenas, the
+            # same rows, are copied from them on the device (dup_rows)
             ins, outs = [], [(h_out[f"c5s{W}"], w.c5_out[W])]
             for r in range(W):
-                src = w.h_c5[W][r * C5_N:(r + 1) * C5_N]
-                ins += [(w.c5_sum_src[W][r], src), (w.c5_ar[W][r], src)]
+                ins.append((w.c5_sum_src[W][r], w.h_c5[W][r * C5_N:(r + 1) * C5_N]))
                 outs.append((h_out[f"c5a{W}"][r * C5_N:(r + 1) * C5_N], w.c5_ar[W][r]))
             io[f"c5_w{W}"] = (ins, outs)
         for n in C2_NS:
@@ -1067,6 +1069,8 @@ def run_gpu(args) -> None:
     # runs, into the buffers of a second row that folds them in place too:
     # row -> (receiving row, [(device dst, device src)] of a buffer set)
     dup_rows = {"c4_fused": ("c4_staged", lambda w: [(w.c4s[r], w.c4f[r]) for r in range(C4_W)])}
+    for W in C5_WS:
+        dup_rows[f"c5_w{W}"] = (f"c5_w{W}", lambda w, W=W: [(w.c5_ar[W][r], w.c5_sum_src[W][r]) for r in range(W)])
     dup_bytes = sum(2 * d.numel() * 4 for _, (_, pairs) in dup_rows.items() for d, _ in pairs(wl))
     step_no = [0]
 
@@ -1223,9 +1227,10 @@ def run_gpu(args) -> None:
                 "pipelined": "per-row H2D and D2H streams around one compute stream; two sets of "
                              "device buffers, alternate steps",
                 "device_copies_per_step": dup_bytes,
-                "device_copies_note": "the C4 input crosses the link once; the staged row's in-place "
-                                      "copy of it is made on the device (detfold_broadcast), inside "
-                                      "the timed region",
+                "device_copies_note": "every input crosses the link once: the staged C4 row's and the "
+                                      "C5 all-reduces' in-place copies of inputs another call also "
+                                      "folds are made on the device (detfold_broadcast), inside the "
+                                      "timed region",
                 "bitwise_sampled_words_differing": int(e2e_check),
                 "link_bytes_gbs": round(link_gbs, 1),
                 "passes": {"count": E2E_PASSES, "steps_each": e2e_steps,

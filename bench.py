@@ -1114,8 +1114,10 @@ def run_gpu(args) -> None:
         e2e_step()
     torch.cuda.synchronize()
 
-    def e2e_pass() -> float:
-        """ms per step over one pass of e2e_steps pipelined steps."""
+    def e2e_pass(compute: bool = True) -> float:
+        """ms per step over one pass of e2e_steps pipelined steps (without
+        their kernels when compute is False: the link's time for the same
+        transfers on the same schedule)."""
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         if dist:
@@ -1125,7 +1127,7 @@ def run_gpu(args) -> None:
         for st_ in list(s_h2d.values()) + list(s_d2h.values()):
             st_.wait_event(e0)
         for _ in range(e2e_steps):
-            e2e_step()
+            e2e_step(compute)
         for st_ in list(s_h2d.values()) + list(s_d2h.values()):
             done = torch.cuda.Event()
             done.record(st_)
@@ -1134,28 +1136,17 @@ def run_gpu(args) -> None:
         torch.cuda.synchronize()
         return max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
 
-    # the host link is measured before and after the passes, in this run:
-    # the end-to-end figure is link-bound, so its spread is read against the
-    # link's own rate at the time
-    def copies_only_ms(steps: int = 3) -> tuple[float, float]:
-        """ms of single steps of the same uploads and read-backs with no
-        kernels (fastest, slowest of `steps`): the link's own rate for this
-        step's transfers at this moment."""
-        ts = []
-        for _ in range(steps):
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            e2e_step(compute=False)
-            torch.cuda.synchronize()
-            ts.append((time.perf_counter() - t0) * 1e3)
-        return min(ts), max(ts)
+    # the host link is measured before and after the passes, in this run,
+    # and after each pass the same transfers run as a pass of their own with
+    # no kernels: the end-to-end figure is link-bound, so it is read against
+    # the link's own rate at the time
 
     link_before = host_link_gbs(torch, dev)
     sample = LinkSample(torch, dev)
     pass_ms, pass_link, pass_copies = [], [], []
     for _ in range(E2E_PASSES):
         pass_ms.append(e2e_pass())
-        pass_copies.append(copies_only_ms())
+        pass_copies.append(e2e_pass(compute=False))
         pass_link.append(sample())
     del sample
     e2e_step()  # leave the last results of a real step in the host buffers
@@ -1238,8 +1229,8 @@ def run_gpu(args) -> None:
                            "gbs_max": round(pass_gbs[-1], 1),
                            "each": [{"gbs": round(whole_job_gbs(world, step_bytes, m), 1),
                                      "ms_per_step": round(m, 2),
-                                     "copies_only_ms_min_max": [round(c[0], 2), round(c[1], 2)],
-                                     "of_fastest_copies_only": round(c[0] / m, 3),
+                                     "copies_only_ms_per_step": round(c, 2),
+                                     "copies_only_of_e2e": round(c / m, 3),
                                      "link_step_gbs": round((h2d + d2h) / (m * 1e-3) / 1e9, 1),
                                      "link_sample_both_gbs": round(l, 1)}
                                     for m, c, l in zip(pass_ms, pass_copies, pass_link)]},

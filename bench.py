@@ -596,9 +596,9 @@ def next_rows(torch, df, wl, reps: int = 10, calls: int = 5) -> dict:
 
 def c5_launches(torch, df, wl, sets: int = 12, reps: int = 4, rounds: int = 2) -> dict:
     """Device time per launch at the C5 length (2^20+7 at base + 4 B), each
-    of the row's three calls alone, beside torch's own elementwise kernels
-    at the same length (an add of two rows into a third; an in-place multiply
-    of one row). Each figure comes from a CUDA graph of `reps` x `sets`
+    of the row's three calls alone and the whole row (the three in order),
+    beside torch's own elementwise kernels at the same length (an add of two
+    rows into a third; an in-place multiply of one row). Each figure comes from a CUDA graph of `reps` x `sets`
     back-to-back launches over `sets` buffer sets whose footprint exceeds L2,
     so every launch reads cold data but none pays a host launch; median of 9
     replays, the best of `rounds` interleaved rounds. At this length a
@@ -650,6 +650,13 @@ def c5_launches(torch, df, wl, sets: int = 12, reps: int = 4, rounds: int = 2) -
         nbytes[f"w{W}_sum"] = (W + 1) * n * 4
         nbytes[f"w{W}_mean_pass"] = 2 * n * 4
         nbytes[f"w{W}_allreduce"] = 2 * W * n * 4
+
+        def row(k, W=W, bufs=bufs, m=m):  # the step's C5 row: the three calls in order
+            df.detfold_sum_ptrs(bufs[k][2], bufs[k][0], W, n)
+            df.detfold_scale(bufs[k][2], n, m)
+            df.detfold_loopback_allreduce(bufs[k][1], W, n, m)
+        calls[f"w{W}_row"] = row
+        nbytes[f"w{W}_row"] = nbytes[f"w{W}_sum"] + nbytes[f"w{W}_mean_pass"] + nbytes[f"w{W}_allreduce"]
     tbufs = [torch.randn((3, n), device=dev) for _ in range(sets)]
     calls["torch_add"] = lambda k: torch.add(tbufs[k][0], tbufs[k][1], out=tbufs[k][2])
     calls["torch_mul_inplace"] = lambda k: tbufs[k][2].mul_(0.5)
@@ -660,7 +667,9 @@ def c5_launches(torch, df, wl, sets: int = 12, reps: int = 4, rounds: int = 2) -
         for key, fn in calls.items():
             us = per_launch_us(fn)
             best[key] = min(best.get(key, us), us)
-    out = {key: {"us": round(us, 3), "gbs": round(nbytes[key] / (us * 1e-6) / 1e9, 1)}
+    peak, _ = peaks()
+    out = {key: {"us": round(us, 3), "gbs": round(nbytes[key] / (us * 1e-6) / 1e9, 1),
+                 "frac": round(nbytes[key] / (us * 1e-6) / 1e9 / peak, 4)}
            for key, us in best.items()}
     out["timing"] = (f"graphs of {reps} x {sets} launches over {sets} buffer sets (cold data), "
                      f"median of 9 replays, best of {rounds} rounds")

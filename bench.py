@@ -108,6 +108,12 @@ def row_bytes() -> dict[str, int]:
     return b
 
 
+def step_input_bytes() -> int:
+    """Bytes of a step's distinct host inputs: the C3 stack, the C4 arenas,
+    the C5 rows and the C2 rows, each counted once."""
+    return 4 * (C3_W * C3_N + C4_W * C4_N + sum(W * C5_N for W in C5_WS) + sum(2 * n for n in C2_NS))
+
+
 def peaks() -> tuple[float, str]:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -1064,6 +1070,8 @@ def run_gpu(args) -> None:
     sets.append((twin, twin.rows(), io_of(twin)))
     io = sets[0][2]
     h2d = sum(d.numel() * 4 for ins, _ in io.values() for d, _ in ins)
+    # every input crosses the link once per step, no more
+    assert h2d == step_input_bytes(), (h2d, step_input_bytes())
     d2h = sum(h.numel() * 4 for _, outs in io.values() for h, _ in outs)
     # one upload and one download stream per row: a row whose buffers are
     # still being read back does not hold up the other rows' uploads

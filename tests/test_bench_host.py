@@ -20,6 +20,14 @@ def test_row_bytes_follow_the_algorithmic_formulas():
     assert b["c2_4096"] == 3 * 4096 * 4
 
 
+def test_step_input_bytes_count_each_input_once():
+    # the end-to-end leg uploads exactly these bytes per step (asserted in
+    # bench.py): C3 8 x 2^26, C4 4 x 1e8, C5 (3 + 6) x (2^20 + 7), C2 2 x n
+    n5 = (1 << 20) + 7
+    want = 4 * (8 * (1 << 26) + 4 * 100_000_000 + 9 * n5 + 2 * (4096 + 65536))
+    assert bench.step_input_bytes() == want == 3_785_789_692
+
+
 def test_kernel_hash_covers_existing_files_and_is_stable():
     h1, h2 = bench.kernel_source_hash(), bench.kernel_source_hash()
     assert h1 == h2 and len(h1) == 16

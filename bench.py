@@ -64,11 +64,11 @@ E2E_PASSES = 5  # end-to-end passes; `e2e.value` is their median
 NCU_TRAFFIC = {
     # profiles/fold_bulk_kernel_W8_sum.md: full-size C3 launch (8 x 2^26),
     # dram__bytes_read.sum + dram__bytes_write.sum
-    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147640064 + 259569664,
-                                  "kernel_hash": "49dc394bce5c6240"},
+    "fold_bulk_kernel<W=8,sum>": {"bytes_per_launch": 2147553536 + 259127552,
+                                  "kernel_hash": "189637e941c52b05"},
     # profiles/fold_bulk_kernel_W4_allreduce.md: full-size C4 launch (4 x 1e8)
-    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600091904 + 1538560000,
-                                         "kernel_hash": "49dc394bce5c6240"},
+    "fold_bulk_kernel<W=4,all-reduce>": {"bytes_per_launch": 1600032000 + 1538591744,
+                                         "kernel_hash": "189637e941c52b05"},
 }
 
 KERNEL_FILES = ("detfold_kernels.cuh", "detfold_launch.cuh", "detfold_async.cuh", "fold_sum_nc.cu",
